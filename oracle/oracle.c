@@ -1,0 +1,547 @@
+/*
+ * Reference oracle (TEST INFRASTRUCTURE ONLY) -- see oracle.h for the page
+ * titles, layouts and the contract of every function.  Slow on purpose: one
+ * thread, double precision, no blocking, the steps in the pages' order.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* element decoding                                                          */
+/* ------------------------------------------------------------------------ */
+
+static size_t esize(int dt) {
+    switch (dt) {
+    case ORC_F32: return 4;
+    case ORC_BF16: return 2;
+    case ORC_F16: return 2;
+    case ORC_I8: return 1;
+    default: return 0;
+    }
+}
+
+/* IEEE binary16 -> double, written out from the format's definition. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int m = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexp(1.0 + m / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* value of element i of a floating-point array of dtype dt */
+static double dec(const void* base, int dt, size_t i) {
+    switch (dt) {
+    case ORC_F32: return (double)((const float*)base)[i];
+    case ORC_BF16: return bf16_bits_to_double(((const uint16_t*)base)[i]);
+    case ORC_F16: return half_bits_to_double(((const uint16_t*)base)[i]);
+    default: return NAN;
+    }
+}
+
+/* the same as fp32 (exact for all three float dtypes) */
+static float decf(const void* base, int dt, size_t i) { return (float)dec(base, dt, i); }
+
+static int is_float_dt(int dt) { return dt == ORC_F32 || dt == ORC_BF16 || dt == ORC_F16; }
+
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+/* ------------------------------------------------------------------------ */
+/* a1: metadata (Quest-ops, 'quest_prefill_metadata: metadata construction')  */
+/* ------------------------------------------------------------------------ */
+
+/* Total order used for max/min: -0 sorts below +0 (IEEE 754-2019
+ * maximum/minimum).  The pages do not discuss signed zero; this reading makes
+ * max/min independent of the reduction order. */
+static int less_total(double a, double b) {
+    if (a < b) return 1;
+    if (a == b && signbit(a) && !signbit(b)) return 1;
+    return 0;
+}
+
+int orc_prefill_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int BS,
+                         int N, int D, const int32_t* seq_lens, int B,
+                         const int32_t* block_tables, int MKBPR,
+                         const int32_t* meta_block_tables, int MMBPR,
+                         int num_meta_blocks, void* maxblocks, void* minblocks) {
+    if (!is_float_dt(kv_dt) || BS <= 0 || N <= 0 || D <= 0 || B < 0 || MKBPR < 0 ||
+        MMBPR < 0)
+        return ORC_EINVAL;
+    const size_t es = esize(kv_dt);
+    const size_t row = (size_t)N * D; /* elements of one token (all heads) */
+    for (int b = 0; b < B; b++) {
+        const int L = seq_lens[b];
+        if (L < 0 || L > MKBPR * BS) return ORC_EINVAL;
+        const int nb = ceil_div(L, BS);
+        const int n_meta = ceil_div(nb, BS);
+        if (n_meta > MMBPR) return ORC_EINVAL;
+        for (int ms = 0; ms < n_meta; ms++) {
+            const int m = meta_block_tables[(size_t)b * MMBPR + ms];
+            if (m < 0 || m >= num_meta_blocks) return ORC_ERANGE;
+            for (int r = 0; r < BS; r++) {
+                const int j = ms * BS + r; /* in-sequence KV block */
+                const size_t out_row = ((size_t)m * BS + r) * row;
+                if (j >= nb) {
+                    /* absent KV block: zero metadata ('tail zero fill') */
+                    memset((char*)maxblocks + out_row * es, 0, row * es);
+                    memset((char*)minblocks + out_row * es, 0, row * es);
+                    continue;
+                }
+                const int p = block_tables[(size_t)b * MKBPR + j];
+                if (p < 0 || p >= num_kv_blocks) return ORC_ERANGE;
+                int valid = L - j * BS;
+                if (valid > BS) valid = BS;
+                for (int n = 0; n < N; n++) {
+                    for (int d = 0; d < D; d++) {
+                        /* channel-wise reduce over the block's valid tokens */
+                        size_t imax = ((size_t)p * BS) * row + (size_t)n * D + d;
+                        size_t imin = imax;
+                        double vmax = dec(k_cache, kv_dt, imax), vmin = vmax;
+                        for (int t = 1; t < valid; t++) {
+                            size_t i = ((size_t)p * BS + t) * row + (size_t)n * D + d;
+                            double v = dec(k_cache, kv_dt, i);
+                            if (less_total(vmax, v)) { vmax = v; imax = i; }
+                            if (less_total(v, vmin)) { vmin = v; imin = i; }
+                        }
+                        size_t o = out_row + (size_t)n * D + d;
+                        memcpy((char*)maxblocks + o * es, (const char*)k_cache + imax * es, es);
+                        memcpy((char*)minblocks + o * es, (const char*)k_cache + imin * es, es);
+                    }
+                }
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a2: group-mean query (Quest-ops, decode-time algorithm, step 1)            */
+/* ------------------------------------------------------------------------ */
+
+int orc_group_mean_query(const void* q, int q_dt, int B, int H, int N, int D,
+                         double* qg) {
+    if (!is_float_dt(q_dt) || N <= 0 || H <= 0 || H % N != 0 || D <= 0) return ORC_EINVAL;
+    const int G = H / N; /* every group of H/N consecutive query heads */
+    for (int b = 0; b < B; b++)
+        for (int n = 0; n < N; n++)
+            for (int d = 0; d < D; d++) {
+                double s = 0.0;
+                for (int g = 0; g < G; g++)
+                    s += dec(q, q_dt, ((size_t)b * H + (size_t)n * G + g) * D + d);
+                qg[((size_t)b * N + n) * D + d] = s / G;
+            }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a3: Quest block score (Quest-ops, decode-time algorithm, steps 2.1-2.2)    */
+/* ------------------------------------------------------------------------ */
+
+int orc_quest_scores(const double* qg, const void* maxblocks, const void* minblocks,
+                     int meta_dt, const int32_t* meta_block_tables, int MMBPR,
+                     int num_meta_blocks, const int32_t* seq_lens, int B, int N,
+                     int D, int BS, double* scores, double* abs_out) {
+    if (!is_float_dt(meta_dt) || BS <= 0 || N <= 0 || D <= 0) return ORC_EINVAL;
+    const int maxnb = MMBPR * BS;
+    for (int b = 0; b < B; b++) {
+        const int L = seq_lens[b];
+        if (L < 0) return ORC_EINVAL;
+        const int nb = ceil_div(L, BS);
+        if (nb > maxnb) return ORC_EINVAL;
+        for (int n = 0; n < N; n++) {
+            const double* g = qg + ((size_t)b * N + n) * D;
+            for (int j = 0; j < nb; j++) {
+                /* 2.1: the metadata block holding row j of this request */
+                const int m = meta_block_tables[(size_t)b * MMBPR + j / BS];
+                if (m < 0 || m >= num_meta_blocks) return ORC_ERANGE;
+                const size_t base = (((size_t)m * BS + j % BS) * N + n) * D;
+                double s = 0.0, sa = 0.0;
+                for (int d = 0; d < D; d++) {
+                    /* 2.2.1 products with the max and min vectors */
+                    double pmax = g[d] * dec(maxblocks, meta_dt, base + d);
+                    double pmin = g[d] * dec(minblocks, meta_dt, base + d);
+                    /* 2.2.2 elementwise max of the two products */
+                    double cmp = pmax > pmin ? pmax : pmin;
+                    /* 2.2.3 reduce-sum over the channel dimension */
+                    s += cmp;
+                    sa += fabs(cmp);
+                }
+                scores[((size_t)b * N + n) * maxnb + j] = s;
+                if (abs_out) abs_out[((size_t)b * N + n) * maxnb + j] = sa;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a4: forced sink + local-window set (Quest-ops, the '_in_out_w' variant)     */
+/* ------------------------------------------------------------------------ */
+
+/* Metadata covers the blocks finished at the last update, which happened
+ * t tokens ago at a multiple of BLOCK_SIZE; blocks from w0 on have no (or
+ * incomplete) metadata and are forced in together with the sink block 0. */
+int orc_forced_set(int seq_len, int BS, int t, int nb, uint8_t* forced) {
+    if (BS <= 0 || nb < 0) return ORC_EINVAL;
+    memset(forced, 0, (size_t)nb);
+    if (t < 0 || nb == 0) return 0;
+    int w0 = (seq_len - t) >= 0 ? (seq_len - t) / BS : 0;
+    if (w0 > nb - 1) w0 = nb - 1;
+    int count = 0;
+    forced[0] = 1;
+    count = 1;
+    for (int j = w0; j < nb; j++)
+        if (!forced[j]) { forced[j] = 1; count++; }
+    return count;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a5: deterministic top-k (Quest-ops step 2.3; tie rule from Kestrel 10-2 §1) */
+/* ------------------------------------------------------------------------ */
+
+static int cmp_int32(const void* a, const void* b) {
+    int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+int orc_quest_select(const void* q, int q_dt, const void* maxblocks,
+                     const void* minblocks, int meta_dt,
+                     const int32_t* meta_block_tables, int MMBPR, int num_meta_blocks,
+                     const int32_t* seq_lens, int B, int H, int N, int D, int BS,
+                     int k, int t, int32_t* selected, float* scores_f32) {
+    if (k <= 0 || N <= 0 || H % N != 0) return ORC_EINVAL;
+    const int maxnb = MMBPR * BS;
+    double* qg = (double*)malloc(sizeof(double) * (size_t)B * N * D + 8);
+    double* sc = (double*)malloc(sizeof(double) * ((size_t)B * N * maxnb + 1));
+    float* sf = (float*)malloc(sizeof(float) * ((size_t)maxnb + 1));
+    uint8_t* used = (uint8_t*)malloc((size_t)maxnb + 1);
+    int32_t* res = (int32_t*)malloc(sizeof(int32_t) * ((size_t)k + 1));
+    int rc = ORC_OK;
+    if (!qg || !sc || !sf || !used || !res) { rc = ORC_EINVAL; goto done; }
+    rc = orc_group_mean_query(q, q_dt, B, H, N, D, qg);
+    if (rc) goto done;
+    rc = orc_quest_scores(qg, maxblocks, minblocks, meta_dt, meta_block_tables, MMBPR,
+                          num_meta_blocks, seq_lens, B, N, D, BS, sc, NULL);
+    if (rc) goto done;
+    for (int b = 0; b < B; b++) {
+        const int L = seq_lens[b];
+        const int nb = ceil_div(L, BS);
+        for (int n = 0; n < N; n++) {
+            /* the top-k ranks the fp32 block scores (the kernels score in fp32) */
+            for (int j = 0; j < nb; j++) {
+                sf[j] = (float)sc[((size_t)b * N + n) * maxnb + j];
+                if (scores_f32) scores_f32[((size_t)b * N + n) * maxnb + j] = sf[j];
+            }
+            int nf = orc_forced_set(L, BS, t, nb, used);
+            if (nf < 0) { rc = nf; goto done; }
+            if (nf > k) { rc = ORC_EFORCED; goto done; }
+            int cnt = 0;
+            for (int j = 0; j < nb; j++)
+                if (used[j]) res[cnt++] = j;
+            /* greedy: repeatedly take the best unused block, ties to the lower
+             * block index, no randomness */
+            while (cnt < k) {
+                int best = -1;
+                for (int j = 0; j < nb; j++) {
+                    if (used[j]) continue;
+                    if (best < 0 || sf[j] > sf[best]) best = j;
+                }
+                if (best < 0) break; /* fewer blocks than k: stop, no padding */
+                used[best] = 1;
+                res[cnt++] = best;
+            }
+            qsort(res, (size_t)cnt, sizeof(int32_t), cmp_int32);
+            int32_t* out = selected + ((size_t)b * N + n) * k;
+            for (int i = 0; i < k; i++) out[i] = i < cnt ? res[i] : -1;
+        }
+    }
+done:
+    free(qg); free(sc); free(sf); free(used); free(res);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* int8 query quantisation (reading of Kestrel 10-2 §2: "q8 KV takes an int8 x  */
+/* int8 dot + scale"; the pages leave the query side open)                    */
+/* ------------------------------------------------------------------------ */
+
+int orc_quantize_query(const void* q, int q_dt, int D, int8_t* q8, float* s_q) {
+    if (!is_float_dt(q_dt) || D <= 0) return ORC_EINVAL;
+    float amax = 0.0f;
+    for (int d = 0; d < D; d++) {
+        float a = fabsf(decf(q, q_dt, (size_t)d));
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+        *s_q = 0.0f;
+        for (int d = 0; d < D; d++) q8[d] = 0;
+        return ORC_OK;
+    }
+    const float s = amax / 127.0f; /* fp32, round to nearest */
+    *s_q = s;
+    for (int d = 0; d < D; d++) {
+        float r = rintf(decf(q, q_dt, (size_t)d) / s); /* half-even */
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        q8[d] = (int8_t)r;
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a6..a8: probe / importance selector (Kestrel 10-2, §1 and §2)              */
+/* ------------------------------------------------------------------------ */
+
+int orc_probe_select(const void* q, int q_dt, const void* k_cache,
+                     const float* k_scale, int kv_dt, int num_kv_blocks,
+                     const int32_t* block_tables, int MKBPR, const int32_t* seq_lens,
+                     const float* importance, int S_max, int B, int H, int N, int D,
+                     int BS, int k, int n_probe, int32_t* selected, float* probe_out,
+                     float* imp_out, int32_t* n_imp_out) {
+    if (k <= 0 || N <= 0 || H % N != 0 || D <= 0 || BS <= 0) return ORC_EINVAL;
+    if (kv_dt == ORC_I8 && !k_scale) return ORC_EINVAL;
+    if (kv_dt != ORC_I8 && !is_float_dt(kv_dt)) return ORC_EINVAL;
+    const int G = H / N;
+    const int maxnb = MKBPR;
+    float* probe = (float*)malloc(sizeof(float) * ((size_t)maxnb + 1));
+    float* imp_sum = (float*)malloc(sizeof(float) * ((size_t)maxnb + 1));
+    uint8_t* used = (uint8_t*)malloc((size_t)maxnb + 1);
+    uint8_t* is_probe_pick = (uint8_t*)malloc((size_t)k + 1);
+    int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * ((size_t)k + 1));
+    float* qf = (float*)malloc(sizeof(float) * (size_t)D);
+    int8_t* q8 = (int8_t*)malloc((size_t)D);
+    int rc = ORC_OK;
+    if (!probe || !imp_sum || !used || !is_probe_pick || !sel || !qf || !q8) {
+        rc = ORC_EINVAL;
+        goto done;
+    }
+    if (n_probe < 1) n_probe = 1;
+    for (int b = 0; b < B; b++) {
+        const int L = seq_lens[b];
+        if (L < 0 || L > MKBPR * BS) { rc = ORC_EINVAL; goto done; }
+        if (importance && L > S_max) { rc = ORC_EINVAL; goto done; }
+        const int n_blocks = ceil_div(L, BS);
+        for (int h = 0; h < H; h++) {
+            const int kh = h / G;
+            const size_t qoff = ((size_t)b * H + h) * D;
+            float s_q = 0.0f;
+            for (int d = 0; d < D; d++) qf[d] = decf(q, q_dt, qoff + d);
+            if (kv_dt == ORC_I8) orc_quantize_query(qf, ORC_F32, D, q8, &s_q);
+
+            /* probe loop: n_probe evenly strided positions per block, block
+             * score = the largest of their dot products */
+            for (int j = 0; j < n_blocks; j++) {
+                float best = -1e30f;
+                const int p0 = j * BS;
+                int p_end = p0 + BS;
+                if (p_end > L) p_end = L;
+                int step = (p_end - p0) / n_probe;
+                if (step < 1) step = 1;
+                const int p = block_tables[(size_t)b * MKBPR + j];
+                if (p < 0 || p >= num_kv_blocks) { rc = ORC_ERANGE; goto done; }
+                for (int ps = p0; ps < p_end; ps += step) {
+                    const size_t krow = (((size_t)p * BS + (ps - p0)) * N + kh) * D;
+                    float dot;
+                    if (kv_dt == ORC_I8) {
+                        long long acc = 0;
+                        for (int d = 0; d < D; d++)
+                            acc += (long long)q8[d] * ((const int8_t*)k_cache)[krow + d];
+                        const float s_k = k_scale[((size_t)p * BS + (ps - p0)) * N + kh];
+                        dot = (s_q * s_k) * (float)acc; /* two fp32 roundings */
+                    } else {
+                        double acc = 0.0;
+                        for (int d = 0; d < D; d++)
+                            acc += (double)qf[d] * dec(k_cache, kv_dt, krow + d);
+                        dot = (float)acc;
+                    }
+                    if (dot > best) best = dot;
+                }
+                probe[j] = best;
+                /* summed prefill importance of the block's tokens, fp32 in
+                 * token order */
+                imp_sum[j] = 0.0f;
+                if (importance)
+                    for (int ps = p0; ps < p_end; ps++)
+                        imp_sum[j] += importance[(size_t)b * S_max + ps];
+                if (probe_out) probe_out[((size_t)b * H + h) * maxnb + j] = probe[j];
+                if (imp_out && h == 0) imp_out[(size_t)b * maxnb + j] = imp_sum[j];
+            }
+
+            memset(used, 0, (size_t)n_blocks + 1);
+            int n_sel = 0;
+            /* importance pre-selection: (k+1)/2 blocks, greedy argmax of the
+             * summed importance, ties to the lower index */
+            int n_imp = 0;
+            if (importance) {
+                const int budget = (k + 1) / 2;
+                for (int i = 0; i < n_blocks && n_imp < budget; i++) {
+                    int best = -1;
+                    for (int j = 0; j < n_blocks; j++) {
+                        if (used[j]) continue;
+                        if (best < 0 || imp_sum[j] > imp_sum[best] ||
+                            (imp_sum[j] == imp_sum[best] && j < best))
+                            best = j;
+                    }
+                    if (best < 0) break;
+                    is_probe_pick[n_imp] = 0;
+                    sel[n_imp++] = best;
+                    used[best] = 1;
+                }
+            }
+            n_sel = n_imp;
+            /* fill the rest greedily by probe score, ties to the lower index;
+             * stop when no block is left (never pad) */
+            while (n_sel < k) {
+                int best = -1;
+                for (int j = 0; j < n_blocks; j++) {
+                    if (used[j]) continue;
+                    if (best < 0 || probe[j] > probe[best] ||
+                        (probe[j] == probe[best] && j < best))
+                        best = j;
+                }
+                if (best < 0) break;
+                is_probe_pick[n_sel] = 1;
+                sel[n_sel++] = best;
+                used[best] = 1;
+            }
+            /* recency insurance: the last block replaces the lowest-scoring
+             * probe pick (ties: the later greedy pick, i.e. the larger index);
+             * importance picks are never evicted */
+            if (n_blocks > 0 && !used[n_blocks - 1]) {
+                int worst = -1;
+                for (int i = 0; i < n_sel; i++) {
+                    if (!is_probe_pick[i]) continue;
+                    if (worst < 0 || probe[sel[i]] < probe[sel[worst]] ||
+                        (probe[sel[i]] == probe[sel[worst]] && sel[i] > sel[worst]))
+                        worst = i;
+                }
+                if (worst >= 0) {
+                    used[sel[worst]] = 0;
+                    sel[worst] = n_blocks - 1;
+                    used[n_blocks - 1] = 1;
+                }
+            }
+            qsort(sel, (size_t)n_sel, sizeof(int32_t), cmp_int32);
+            int32_t* out = selected + ((size_t)b * H + h) * k;
+            for (int i = 0; i < k; i++) out[i] = i < n_sel ? sel[i] : -1;
+            if (n_imp_out) n_imp_out[(size_t)b * H + h] = n_imp;
+        }
+    }
+done:
+    free(probe); free(imp_sum); free(used); free(is_probe_pick); free(sel); free(qf);
+    free(q8);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* a9: exact attention over the selected blocks (Kestrel 10-2 §1, the cost     */
+/* paragraph: softmax renormalised over the selected blocks only; Quest-ops:  */
+/* indices are in-sequence and go through block_tables)                      */
+/* ------------------------------------------------------------------------ */
+
+int orc_sparse_attention(const void* q, int q_dt, const void* k_cache,
+                         const void* v_cache, const float* k_scale,
+                         const float* v_scale, int kv_dt, int num_kv_blocks,
+                         const int32_t* block_tables, int MKBPR,
+                         const int32_t* seq_lens, const int32_t* selected,
+                         int sel_heads, int k, double softmax_scale, int B, int H,
+                         int N, int D, int BS, double* out, double* lse) {
+    if (k <= 0 || N <= 0 || H % N != 0 || D <= 0 || BS <= 0) return ORC_EINVAL;
+    if (sel_heads != N && sel_heads != H) return ORC_EINVAL;
+    if (kv_dt == ORC_I8 && (!k_scale || !v_scale)) return ORC_EINVAL;
+    if (kv_dt != ORC_I8 && !is_float_dt(kv_dt)) return ORC_EINVAL;
+    const int G = H / N;
+    const size_t max_tok = (size_t)k * BS;
+    double* logit = (double*)malloc(sizeof(double) * (max_tok + 1));
+    size_t* vrow = (size_t*)malloc(sizeof(size_t) * (max_tok + 1));
+    size_t* srow = (size_t*)malloc(sizeof(size_t) * (max_tok + 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+    float* qf = (float*)malloc(sizeof(float) * (size_t)D);
+    int8_t* q8 = (int8_t*)malloc((size_t)D);
+    int rc = ORC_OK;
+    if (!logit || !vrow || !srow || !qd || !qf || !q8) { rc = ORC_EINVAL; goto done; }
+    for (int b = 0; b < B; b++) {
+        const int L = seq_lens[b];
+        if (L < 0 || L > MKBPR * BS) { rc = ORC_EINVAL; goto done; }
+        const int nb = ceil_div(L, BS);
+        for (int h = 0; h < H; h++) {
+            const int n = h / G;
+            const int s = sel_heads == H ? h : n;
+            const int32_t* row = selected + ((size_t)b * sel_heads + s) * k;
+            const size_t qoff = ((size_t)b * H + h) * D;
+            float s_q = 0.0f;
+            for (int d = 0; d < D; d++) { qd[d] = dec(q, q_dt, qoff + d); qf[d] = (float)qd[d]; }
+            if (kv_dt == ORC_I8) orc_quantize_query(qf, ORC_F32, D, q8, &s_q);
+            /* token scores over the selected blocks only */
+            size_t T = 0;
+            for (int i = 0; i < k; i++) {
+                const int j = row[i];
+                if (j < 0) continue;
+                if (j >= nb) { rc = ORC_ERANGE; goto done; }
+                for (int i2 = 0; i2 < i; i2++)
+                    if (row[i2] == j) { rc = ORC_EDUP; goto done; }
+                const int p = block_tables[(size_t)b * MKBPR + j];
+                if (p < 0 || p >= num_kv_blocks) { rc = ORC_ERANGE; goto done; }
+                int valid = L - j * BS;
+                if (valid > BS) valid = BS;
+                for (int t = 0; t < valid; t++) {
+                    const size_t tok = ((size_t)p * BS + t) * N + n;
+                    const size_t kr = tok * D;
+                    double dot = 0.0;
+                    if (kv_dt == ORC_I8) {
+                        long long acc = 0;
+                        for (int d = 0; d < D; d++)
+                            acc += (long long)q8[d] * ((const int8_t*)k_cache)[kr + d];
+                        dot = (double)s_q * (double)k_scale[tok] * (double)acc;
+                    } else {
+                        for (int d = 0; d < D; d++) dot += qd[d] * dec(k_cache, kv_dt, kr + d);
+                    }
+                    logit[T] = softmax_scale * dot;
+                    vrow[T] = kr;
+                    srow[T] = tok;
+                    T++;
+                }
+            }
+            double* o = out + qoff;
+            if (T == 0) {
+                for (int d = 0; d < D; d++) o[d] = 0.0;
+                if (lse) lse[(size_t)b * H + h] = -INFINITY;
+                continue;
+            }
+            /* softmax over the selected set: subtract the max, normalise */
+            double m = logit[0];
+            for (size_t i = 1; i < T; i++) if (logit[i] > m) m = logit[i];
+            double l = 0.0;
+            for (size_t i = 0; i < T; i++) { logit[i] = exp(logit[i] - m); l += logit[i]; }
+            /* weighted sum of V */
+            for (int d = 0; d < D; d++) {
+                double acc = 0.0;
+                for (size_t i = 0; i < T; i++) {
+                    double v = kv_dt == ORC_I8
+                                   ? (double)((const int8_t*)v_cache)[vrow[i] + d] * (double)v_scale[srow[i]]
+                                   : dec(v_cache, kv_dt, vrow[i] + d);
+                    acc += logit[i] * v;
+                }
+                o[d] = acc / l;
+            }
+            if (lse) lse[(size_t)b * H + h] = m + log(l);
+        }
+    }
+done:
+    free(logit); free(vrow); free(srow); free(qd); free(qf); free(q8);
+    return rc;
+}
