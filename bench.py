@@ -1,0 +1,545 @@
+"""Decode-step benchmark: select + sparse decode attention on one GB300.
+
+One step = the whole hot path over one batch: block selection (Quest, or the
+probe/importance selector) followed by the split-K sparse attention, enqueued
+through the C ABI (qs_sparse_decode_step) and replayed as a CUDA graph.  The
+metadata prefill is set-up, timed separately and reported on its own.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream, with a 256 MiB write between steps so that no input of a
+step is served from the 129 MB L2.  The dominant kernel (the attention) is
+also timed alone the same way for the roofline.  Under torchrun every rank
+runs an independent replica (the path needs no collective) and the slowest
+rank's time is reported.
+
+JSON line keys: metric, value (us per step, lower is better), unit, roofline
+(attention kernel vs the measured HBM copy bandwidth), cpu_baseline (the
+reference oracle on the host, bounded sample), e2e (the same step through the
+C ABI from pinned host buffers, copies included), clocks, gpu_launches.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from decode_sparse_attention_gb300 import synth  # noqa: E402
+
+METRIC = "select+sparse decode-attn µs/step and achieved HBM GB/s (% of peak), 1×GB300"
+UNIT = "us/step"
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas; CPU-testable with gloo)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank float over the process group (identity without one)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (per step) -- the counting rule of the design notes
+# ---------------------------------------------------------------------------
+
+def elem_bytes(dtype):
+    return {torch.float32: 4, torch.bfloat16: 2, torch.float16: 2, torch.int8: 1}[dtype]
+
+
+def selected_kv_bytes(sel: np.ndarray, seq_lens: np.ndarray, w, kv_es: int, int8: bool) -> int:
+    """K and V bytes of the valid tokens of the selected blocks, each block
+    counted once per KV head (the union over the group's query heads)."""
+    total_tok = 0
+    rows = sel.shape[1]
+    for b in range(sel.shape[0]):
+        L = int(seq_lens[b])
+        if rows == w.N:
+            groups = [[n] for n in range(w.N)]
+        else:
+            groups = [list(range(n * w.G, (n + 1) * w.G)) for n in range(w.N)]
+        for grp in groups:
+            blocks = set()
+            for r in grp:
+                blocks.update(int(j) for j in sel[b, r] if j >= 0)
+            for j in blocks:
+                total_tok += max(0, min(w.BS, L - j * w.BS))
+    per_tok = w.D * kv_es * 2 + (8 if int8 else 0)
+    return total_tok * per_tok
+
+
+def step_bytes(w, x, sel, q_es):
+    L = x["seq_lens"].cpu().numpy()
+    kv_es = elem_bytes(x["k_cache"].dtype)
+    int8 = x["k_cache"].dtype == torch.int8
+    q = w.B * w.H * w.D * q_es
+    kv = selected_kv_bytes(sel, L, w, kv_es, int8)
+    idx = sel.size * 4
+    out = w.B * w.H * w.D * 4
+    if w.mode == "quest":
+        rows = sum((int(l) + w.BS - 1) // w.BS for l in L)
+        select = rows * w.N * w.D * kv_es * 2
+    else:
+        # probed K rows + the importance of every token
+        select = 0
+        for l in L:
+            nb = (int(l) + w.BS - 1) // w.BS
+            for j in range(nb):
+                valid = min(w.BS, int(l) - j * w.BS)
+                step = max(1, valid // max(w.n_probe, 1))
+                select += len(range(0, valid, step)) * w.N * (w.D * kv_es + (4 if int8 else 0))
+        if w.importance:
+            select += int(L.sum()) * 4
+    return {"q": q, "select": select, "kv": kv, "indices": idx, "out": out,
+            "step": q + select + kv + idx + out, "attention": q + kv + idx + out}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + CLOCK_QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() in ("active", "0x1", "1"):
+                        reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# peaks and committed ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("qs_attention.cu", "qs_common.cuh"):
+        with open(os.path.join(ROOT, "decode_sparse_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """dram read+write bytes per attention launch from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "sparse_attn_%s.md" % workload)
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_val = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
+    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_val.group(1))
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+def setup(w, seed, dev):
+    from decode_sparse_attention_gb300 import questsparse as qs
+    x = synth.make(w, seed=seed, device=dev)
+    mode = 0 if w.mode == "quest" else 1
+    meta_ms = None
+    if mode == 0:
+        # metadata prefill: set-up of the step, timed on its own
+        for _ in range(2):
+            qs.quest_prefill_metadata(x["k_cache"], x["meta_seq_lens"], x["block_tables"],
+                                      x["meta_block_tables"], x["maxblocks"], x["minblocks"])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        qs.quest_prefill_metadata(x["k_cache"], x["meta_seq_lens"], x["block_tables"],
+                                  x["meta_block_tables"], x["maxblocks"], x["minblocks"])
+        e1.record()
+        torch.cuda.synchronize()
+        meta_ms = e0.elapsed_time(e1)
+    rows = w.N if mode == 0 else w.H
+    sel = torch.full((w.B, rows, w.k), -1, dtype=torch.int32, device=dev)
+    out = torch.empty((w.B, w.H, w.D), dtype=torch.float32, device=dev)
+    nbytes = qs.step_workspace_bytes(mode, w.B, w.H, w.N, w.D, w.BS, w.k,
+                                     MMBPR=x["meta_block_tables"].shape[1], MKBPR=x["MKBPR"])
+    ws = qs.workspace(nbytes, dev, "bench-step")
+    params = qs.make_step_params(mode, x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                                 x["seq_lens"], w.k, sel, out, ws, maxblocks=x.get("maxblocks"),
+                                 minblocks=x.get("minblocks"),
+                                 metadata_block_tables=x["meta_block_tables"],
+                                 tokens_since_metadata_update=x["t"],
+                                 importance=x.get("importance"), n_probe=w.n_probe,
+                                 k_scale=x.get("k_scale"), v_scale=x.get("v_scale"))
+    return x, mode, sel, out, params, meta_ms
+
+
+def timed_graph(graph, flush, steps, stream):
+    """Per-step CUDA-event durations (ms) of graph replays with an L2 flush
+    between steps."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        graph.replay()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def run_ours(args, w):
+    from decode_sparse_attention_gb300 import questsparse as qs
+    ws_, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    qs.lib()
+    x, mode, sel, out, params, meta_ms = setup(w, args.seed + rank, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    # eager warm-up, then capture the step in a graph
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            qs.sparse_decode_step(params, dev)
+    torch.cuda.synchronize()
+    assert qs.read_status(dev) == 0
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        qs.sparse_decode_step(params, dev)
+    # the dominant kernel alone (same selection, same launch configuration)
+    attn_out = torch.empty_like(out)
+    g_attn = torch.cuda.CUDAGraph()
+    sel_rows = sel.shape[1]
+    with torch.cuda.graph(g_attn, stream=stream):
+        qs.sparse_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                              x["seq_lens"], sel, k_scale=x.get("k_scale"),
+                              v_scale=x.get("v_scale"), out=attn_out)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    t_end = time.time() + 1.5
+    for _ in range(args.warmup):
+        flush.zero_()
+        g_step.replay()
+    while time.time() < t_end:      # keep the clocks under load for the sampler
+        g_step.replay()
+    torch.cuda.synchronize()
+    barrier()
+    durs = timed_graph(g_step, flush, args.steps, stream)
+    barrier()
+    attn_durs = timed_graph(g_attn, flush, max(args.steps // 2, 3), stream)
+    clocks = sampler.stop()
+    assert qs.read_status(dev) == 0
+
+    step_us = 1000.0 * sum(durs) / len(durs)
+    attn_us = 1000.0 * sum(attn_durs) / len(attn_durs)
+    step_us_max = max_over_ranks(step_us, dev)
+    sel_np = sel.cpu().numpy()
+    q_es = elem_bytes(x["q"].dtype)
+    nbytes = step_bytes(w, x, sel_np, q_es)
+
+    # end to end through the C ABI from pinned host buffers
+    host = {k: x[k].cpu().pin_memory() for k in ("q", "seq_lens", "block_tables",
+                                                 "meta_block_tables")}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ms = []
+    for i in range(max(args.steps // 4, 3) + 3):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for k_, v in host.items():
+                x[k_].copy_(v, non_blocking=True)
+            qs.sparse_decode_step(params, dev)
+            host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+        if i >= 3:
+            e2e_ms.append(1000.0 * (time.perf_counter() - t0))
+    e2e_us = max_over_ranks(1000.0 * statistics.median(e2e_ms), dev)
+
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes["attention"] / (attn_us * 1e-6) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(step_us_max, 3),
+        "unit": UNIT,
+        "n_gpus": ws_,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_us_max / 1000.0, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16",
+                  torch.int8: "i8"}[x["k_cache"].dtype],
+        "data": "synthetic",
+        "config": {
+            "workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "block_size": w.BS,
+            "seq_len": w.seq_len if w.seq_len else "ragged", "k": w.k,
+            "tokens_since_metadata_update": x["t"], "selector": w.mode,
+            "parallelism": "replicas" if ws_ > 1 else "single GPU",
+            "l2": "256 MiB write between timed steps",
+            "step": "qs_sparse_decode_step replayed as a CUDA graph",
+        },
+        "step_gbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9, 1),
+        "step_frac_of_peak": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / peak, 4),
+        "step_frac_of_8tbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / 8000.0, 4),
+        "algorithmic_bytes": nbytes,
+        "step_us_p10_p50_p90": [round(1000 * float(np.percentile(durs, p)), 3) for p in (10, 50, 90)],
+        "roofline": {
+            "kernel": "sparse_attn_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": committed_traffic(w.name),
+            "launch_us": round(attn_us, 3),
+            "bytes_per_launch": nbytes["attention"],
+        },
+        "metadata_prefill_us": None if meta_ms is None else round(meta_ms * 1000, 2),
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+    }
+    if meta_ms is not None:
+        L = x["meta_seq_lens"].cpu().numpy()
+        kbytes = int(sum(int(l) for l in L)) * w.N * w.D * elem_bytes(x["k_cache"].dtype)
+        mrows = sum(((int(l) + w.BS - 1) // w.BS + w.BS - 1) // w.BS * w.BS for l in x["seq_lens"].cpu().numpy())
+        mbytes = mrows * w.N * w.D * elem_bytes(x["k_cache"].dtype) * 2
+        res["metadata_prefill_gbs"] = round((kbytes + mbytes) / (meta_ms * 1e-3) / 1e9, 1)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return res if rank == 0 else None
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host (CPU baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _np_bits(t):
+    t = t.detach().cpu().contiguous()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def oracle_inputs(w, x, reqs):
+    """Host copies of the sampled requests (their pages renumbered), with the
+    oracle's own metadata for the Quest selector (built untimed: it is set-up)."""
+    import oracle
+    bt = x["block_tables"].cpu().numpy()[reqs]
+    pages = sorted(set(int(p) for p in bt.ravel() if p >= 0))
+    remap = {p: i for i, p in enumerate(pages)}
+    bt2 = np.vectorize(lambda p: remap.get(int(p), -1))(bt).astype(np.int32)
+    idx = torch.tensor(pages, dtype=torch.long, device=x["k_cache"].device)
+    sub = {"q": _np_bits(x["q"][reqs]), "seq_lens": x["seq_lens"].cpu().numpy()[reqs],
+           "k": _np_bits(x["k_cache"][idx]), "v": _np_bits(x["v_cache"][idx]), "bt": bt2}
+    dt = {torch.float32: oracle.F32, torch.bfloat16: oracle.BF16, torch.float16: oracle.F16,
+          torch.int8: oracle.I8}
+    sub["q_dt"], sub["kv_dt"] = dt[x["q"].dtype], dt[x["k_cache"].dtype]
+    if "k_scale" in x:
+        sub["ks"], sub["vs"] = x["k_scale"][idx].cpu().numpy(), x["v_scale"][idx].cpu().numpy()
+    if "importance" in x:
+        sub["imp"] = x["importance"][reqs].cpu().numpy()
+    if w.mode == "quest":
+        mbt = x["meta_block_tables"].cpu().numpy()[reqs]
+        n_meta = int((mbt >= 0).sum())
+        mbt2 = np.full_like(mbt, -1)
+        c = 0
+        for r in range(mbt.shape[0]):
+            for s in range(mbt.shape[1]):
+                if mbt[r, s] >= 0:
+                    mbt2[r, s] = c
+                    c += 1
+        shape = (max(n_meta, 1), w.BS, w.N, w.D)
+        mx = np.zeros(shape, sub["k"].dtype)
+        mn = np.zeros(shape, sub["k"].dtype)
+        oracle.prefill_metadata(sub["k"], sub["kv_dt"], x["meta_seq_lens"].cpu().numpy()[reqs],
+                                bt2, mbt2, mx, mn)
+        sub.update(mx=mx, mn=mn, mbt=mbt2)
+    return sub
+
+
+def oracle_step(w, t, sub):
+    import oracle
+    if w.mode == "quest":
+        sel, _ = oracle.quest_select(sub["q"], sub["q_dt"], sub["mx"], sub["mn"], sub["kv_dt"],
+                                     sub["mbt"], sub["seq_lens"], w.N, w.k, t)
+    else:
+        sel, *_ = oracle.probe_select(sub["q"], sub["q_dt"], sub["k"], sub["kv_dt"], sub["bt"],
+                                      sub["seq_lens"], w.N, w.k, w.n_probe,
+                                      importance=sub.get("imp"), k_scale=sub.get("ks"))
+    oracle.sparse_attention(sub["q"], sub["q_dt"], sub["k"], sub["v"], sub["kv_dt"], sub["bt"],
+                            sub["seq_lens"], sel, w.N, k_scale=sub.get("ks"), v_scale=sub.get("vs"))
+
+
+def oracle_sample_reqs(w, x, budget_s):
+    """Requests to run per oracle step: grows until one step takes ~1/8 of the
+    budget (at least one request)."""
+    n = 1
+    while True:
+        reqs = list(range(min(n, w.B)))
+        sub = oracle_inputs(w, x, reqs)
+        t0 = time.perf_counter()
+        oracle_step(w, x["t"], sub)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 8 or n >= w.B:
+            return reqs, sub, dt
+        n = min(w.B, max(n + 1, int(n * budget_s / 8 / max(dt, 1e-4))))
+
+
+def cpu_baseline(w, x, budget_s):
+    reqs, sub, _ = oracle_sample_reqs(w, x, budget_s)
+    times = []
+    t_stop = time.perf_counter() + budget_s
+    while time.perf_counter() < t_stop or len(times) < 2:
+        t0 = time.perf_counter()
+        oracle_step(w, x["t"], sub)
+        times.append(time.perf_counter() - t0)
+    per_step_us = statistics.median(times) * 1e6 * w.B / len(reqs)
+    return {"value": round(per_step_us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d of %d requests per step, %d runs, scaled by %d/%d to a full step"
+                      % (len(reqs), w.B, len(times), w.B, len(reqs))}
+
+
+def run_reference(args, w):
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    x = synth.make(w, seed=args.seed, device=dev)
+    reqs, sub, dt = oracle_sample_reqs(w, x, min(args.cpu_seconds, 8.0))
+    for _ in range(args.warmup):
+        oracle_step(w, x["t"], sub)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, x["t"], sub)
+        times.append(time.perf_counter() - t0)
+    us = statistics.mean(times) * 1e6 * w.B / len(reqs)
+    sample = ("oracle (single-threaded C, double) on %d of %d requests per step, scaled by %d/%d"
+              % (len(reqs), w.B, w.B, len(reqs)))
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+            "n_gpus": ws_, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us / 1000, 4), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
+                       "block_size": w.BS, "k": w.k, "selector": w.mode},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16_paged", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+    res = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

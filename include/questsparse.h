@@ -1,0 +1,232 @@
+/*
+ * questsparse -- query-aware sparse KV-block selection and sparse decode
+ * attention for one GB300 (sm_103a) GPU.  C ABI.
+ *
+ * Operations and where they are defined:
+ *   qs_prefill_metadata    CANN ops-transformer select_attention_operators page
+ *                          (Quest on Ascend 910B), section 'quest_prefill_metadata:
+ *                          metadata construction'.
+ *   qs_block_select_paged  same page, section 'quest_block_select_paged: decode-time
+ *                          top-k prediction' (steps 1, 2.1-2.3) and the three
+ *                          interfaces ('_in_out' / '_in_out_w': the sink + window
+ *                          variant driven by tokens_since_metadata_update).
+ *   qs_probe_select        Kestrel-LLM article 10-2 'sparse top-k block selection',
+ *                          sections 1 and 2 (probe loop, (k+1)/2 importance budget,
+ *                          greedy probe fill, recency insurance).
+ *   qs_sparse_decode_attn  Kestrel-LLM 10-2 section 2 (exact attention over the
+ *                          selected blocks only, softmax renormalised over that set)
+ *                          with the in-sequence -> physical mapping through
+ *                          block_tables from the CANN page's top-k section.
+ *   qs_sparse_decode_step  select (either mode) followed by the attention.
+ *
+ * Conventions shared by every call:
+ *  - All tensor arguments are DEVICE pointers to contiguous row-major memory
+ *    owned by the caller.  The library never allocates device memory; the
+ *    scratch a call needs is a caller-provided workspace whose size
+ *    qs_workspace_size() returns.  A workspace must be zero-filled once before
+ *    its first use (and again after a call reported a device-side error); the
+ *    calls leave it zero-filled for the next call.
+ *  - Every call enqueues its kernels on `stream` and returns without waiting.
+ *    The returned qs_status reports host-side validation and launch errors only.
+ *  - Faults found on the device (a table entry out of range, a bad seq_len, an
+ *    out-of-range selected index) do not trap: the kernel skips the bad unit and
+ *    stores the first such code into the caller's int32 `dev_status` word
+ *    (sticky; 0 = no error).  Read it with qs_read_status().
+ *  - Shapes: B requests, H query heads, N KV heads (H % N == 0; query head h
+ *    belongs to KV head h / (H/N)), D head dim, BS tokens per KV block.
+ *      q                    [B, H, D]                 (fp32, bf16 or fp16)
+ *      k_cache, v_cache     [num_kv_blocks, BS, N, D] (fp32, bf16, fp16 or int8)
+ *      k_scale, v_scale     [num_kv_blocks, BS, N]    fp32, int8 caches only:
+ *                           value = int8 * scale, one scale per (token, KV head)
+ *      block_tables         [B, MKBPR] int32, in-sequence block -> physical block
+ *      seq_lens             [B] int32, 0 <= seq_len <= MKBPR * BS
+ *      maxblocks, minblocks [num_meta_blocks, BS, N, D], dtype of the K cache;
+ *                           row r of a request's metadata block slot s holds KV
+ *                           block s*BS + r of that request
+ *      meta_block_tables    [B, MMBPR] int32, request -> metadata blocks
+ *  - Block indices returned by the selectors are IN-SEQUENCE indices (0 is the
+ *    first block of the request), ascending, padded with -1.  A request with
+ *    nb = ceil(seq_len/BS) < k blocks gets nb indices.
+ */
+#ifndef QUESTSPARSE_H
+#define QUESTSPARSE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* qs_stream_t;
+
+typedef enum {
+    QS_OK = 0,
+    QS_EINVAL = 1,        /* bad shape, size, pointer or k                    */
+    QS_EDTYPE = 2,        /* dtype combination not supported by the call      */
+    QS_EUNSUPPORTED = 3,  /* no kernel instantiation for this D / BS / H/N    */
+    QS_ECUDA = 4,         /* a CUDA runtime call or kernel launch failed      */
+    QS_EWORKSPACE = 5     /* workspace missing or smaller than required       */
+} qs_status;
+
+typedef enum { QS_F32 = 0, QS_BF16 = 1, QS_F16 = 2, QS_I8 = 3 } qs_dtype;
+
+/* Codes the kernels store into *dev_status (first error wins). */
+typedef enum {
+    QS_DEV_OK = 0,
+    QS_DEV_EBLOCK_TABLE = 1,  /* block_tables entry outside [0, num_kv_blocks)  */
+    QS_DEV_EMETA_TABLE = 2,   /* meta_block_tables entry outside [0, num_meta)  */
+    QS_DEV_ESEQ_LEN = 3,      /* seq_len < 0 or > MKBPR*BS (or metadata slots)  */
+    QS_DEV_ESELECTED = 4,     /* selected index >= ceil(seq_len/BS)             */
+    QS_DEV_EFORCED = 5,       /* more forced window blocks than k               */
+    QS_DEV_ETIMEOUT = 6       /* a bounded device-side wait ran out             */
+} qs_dev_code;
+
+typedef enum {
+    QS_OP_BLOCK_SELECT = 0,
+    QS_OP_PROBE_SELECT = 1,
+    QS_OP_SPARSE_ATTN = 2,
+    QS_OP_DECODE_STEP_QUEST = 3,
+    QS_OP_DECODE_STEP_PROBE = 4
+} qs_op;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t qs_version(void);
+
+/* Human-readable text for a qs_status or, for values >= 100, for the device
+ * code (value - 100).  Never NULL. */
+const char* qs_status_string(int32_t code);
+
+/* Copies *dev_status to *host_code, waiting for `stream`; resets the device
+ * word to 0 when reset != 0. */
+qs_status qs_read_status(const int32_t* dev_status, int32_t* host_code, int32_t reset,
+                         qs_stream_t stream);
+
+/* Bytes of workspace `op` needs for these sizes (0 is possible).
+ *   max_blocks_per_req: MMBPR*BS for the Quest selector, MKBPR otherwise.
+ *   sel_heads: rows of the selection fed to the attention (N or H). */
+qs_status qs_workspace_size(qs_op op, int32_t B, int32_t H, int32_t N, int32_t D,
+                            int32_t BS, int32_t k, int32_t max_blocks_per_req,
+                            int32_t sel_heads, size_t* bytes);
+
+/*
+ * Quest metadata (CANN page, 'quest_prefill_metadata: metadata construction').
+ * For every request b, in-sequence KV block j < nb_b and KV head n: the
+ * channel-wise max and min of K over the block's valid tokens
+ * (t < min(BS, seq_len - j*BS)), written to row j % BS, head n of metadata
+ * block meta_block_tables[b][j / BS].  Rows j >= nb_b of the metadata blocks
+ * the request uses (slots < ceil(nb_b / BS)) are zero-filled; nothing else is
+ * written.  Max/min are exact (the results are input elements; -0 orders
+ * below +0).  kv_dtype: fp32, bf16 or fp16; maxblocks/minblocks have that
+ * dtype.  MMBPR must be >= ceil(MKBPR / BS).
+ */
+qs_status qs_prefill_metadata(const void* k_cache, qs_dtype kv_dtype, int32_t num_kv_blocks,
+                              int32_t BS, int32_t N, int32_t D, const int32_t* seq_lens,
+                              int32_t B, const int32_t* block_tables, int32_t MKBPR,
+                              const int32_t* meta_block_tables, int32_t MMBPR,
+                              int32_t num_meta_blocks, void* maxblocks, void* minblocks,
+                              int32_t* dev_status, qs_stream_t stream);
+
+/*
+ * Quest block selection (CANN page, 'quest_block_select_paged', steps 1-3).
+ * qg[b][n] = mean of the H/N query heads of group n (fp32); block score
+ * s_j = sum_d max(qg_d*max_jd, qg_d*min_jd) (fp32) for j < nb_b; the top
+ * k - |F| non-forced blocks by (score descending, index ascending) plus the
+ * forced set F, written ascending into selected [B, N, k], -1 padded.
+ * tokens_since_metadata_update = t: t < 0 disables the window (F empty);
+ * t >= 0 forces F = {0} U [w0, nb_b), w0 = min(floor((seq_len - t)/BS), nb_b-1)
+ * (the blocks whose metadata the last update, t tokens ago at a multiple of
+ * BS, did not cover).  Requires k >= 2 + ceil(t/BS) when t >= 0 (|F| bound).
+ * scores_opt: NULL, or [B, N, MMBPR*BS] fp32 that receives s_j for j < nb_b.
+ * q_dtype, meta_dtype: fp32, bf16 or fp16.  D in {64, 128}.
+ */
+qs_status qs_block_select_paged(const void* q, qs_dtype q_dtype, const void* maxblocks,
+                                const void* minblocks, qs_dtype meta_dtype,
+                                const int32_t* meta_block_tables, int32_t MMBPR,
+                                int32_t num_meta_blocks, const int32_t* seq_lens, int32_t B,
+                                int32_t H, int32_t N, int32_t D, int32_t BS, int32_t k,
+                                int32_t tokens_since_metadata_update, int32_t* selected,
+                                float* scores_opt, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, qs_stream_t stream);
+
+/*
+ * Probe / prefill-importance selection (Kestrel-LLM 10-2, sections 1-2), one
+ * selection per QUERY head: selected [B, H, k].
+ *  probe_j = max over positions ps = p0, p0+step, ... < p_end of q_h . K[ps]
+ *           (p0 = j*BS, p_end = min(p0+BS, seq_len), step = max(1,
+ *           (p_end-p0)/n_probe); fp32 dot; int8 caches: (s_q*s_k)*int_dot with
+ *           q quantised per (b,h) as s_q = max|q|/127, q8 = rint(q/s_q)).
+ *  importance: NULL, or [B, importance_stride] fp32 per-token prefill
+ *           importance; imp_j = fp32 sum of the block's tokens in order.
+ *  Picks: (k+1)/2 blocks by importance (ties to the lower index), the rest by
+ *  probe score (ties to the lower index), stopping when blocks run out; then
+ *  if block nb-1 is missing and a probe pick exists, it replaces the probe
+ *  pick with the lowest probe score (ties: the larger index).  Importance
+ *  picks are never evicted.  D in {64, 128}; n_probe >= 1 (values < 1 act as 1).
+ */
+qs_status qs_probe_select(const void* q, qs_dtype q_dtype, const void* k_cache,
+                          const float* k_scale, qs_dtype kv_dtype, int32_t num_kv_blocks,
+                          const int32_t* block_tables, int32_t MKBPR, const int32_t* seq_lens,
+                          const float* importance, int32_t importance_stride, int32_t B,
+                          int32_t H, int32_t N, int32_t D, int32_t BS, int32_t k,
+                          int32_t n_probe, int32_t* selected, void* workspace,
+                          size_t workspace_bytes, int32_t* dev_status, qs_stream_t stream);
+
+/*
+ * Exact decode attention over the selected blocks only (Kestrel-LLM 10-2,
+ * section 2; block indices mapped through block_tables per the CANN page).
+ * For query head h of request b: T = tokens t < min(BS, seq_len - j*BS) of the
+ * blocks j listed in selected[b][s] (s = h / (H/N) when sel_heads == N, s = h
+ * when sel_heads == H; entries < 0 skipped; listed blocks must be distinct),
+ * logits l = softmax_scale * q_h . K (int8: softmax_scale * s_q*s_k * int_dot),
+ * p = softmax of l over T only, out[b][h] = sum p * V (fp32, [B, H, D]).
+ * lse_opt: NULL or [B, H] fp32 natural-log log-sum-exp of the logits.  An
+ * empty T gives out = 0 and lse = -inf.  Split-K over the selected blocks; the
+ * partial results are merged on the device (no host round trip).
+ * D in {64, 128}; BS a multiple of 16, <= 256; H/N (sel_heads == N) in {1,2,4}.
+ */
+qs_status qs_sparse_decode_attn(const void* q, qs_dtype q_dtype, const void* k_cache,
+                                const void* v_cache, const float* k_scale, const float* v_scale,
+                                qs_dtype kv_dtype, int32_t num_kv_blocks,
+                                const int32_t* block_tables, int32_t MKBPR,
+                                const int32_t* seq_lens, const int32_t* selected,
+                                int32_t sel_heads, int32_t k, float softmax_scale, int32_t B,
+                                int32_t H, int32_t N, int32_t D, int32_t BS, float* out,
+                                float* lse_opt, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, qs_stream_t stream);
+
+/* One decode step: a selector followed by the attention, enqueued back to back
+ * on one stream (the attention is launched as a programmatic dependent of the
+ * selector).  Quest mode reads maxblocks/minblocks/meta tables and writes
+ * selected [B, N, k]; probe mode reads importance and writes selected [B, H, k].
+ * The workspace is shared: size it with QS_OP_DECODE_STEP_QUEST/_PROBE. */
+typedef struct {
+    int32_t mode;                    /* 0 = Quest, 1 = probe/importance        */
+    const void* q; qs_dtype q_dtype;
+    const void* k_cache; const void* v_cache;
+    const float* k_scale; const float* v_scale; qs_dtype kv_dtype;
+    int32_t num_kv_blocks;
+    const int32_t* block_tables; int32_t MKBPR;
+    const int32_t* seq_lens;
+    /* Quest mode */
+    const void* maxblocks; const void* minblocks;
+    const int32_t* meta_block_tables; int32_t MMBPR; int32_t num_meta_blocks;
+    int32_t tokens_since_metadata_update;
+    /* probe mode */
+    const float* importance; int32_t importance_stride; int32_t n_probe;
+    /* sizes */
+    int32_t B, H, N, D, BS, k;
+    float softmax_scale;
+    /* outputs */
+    int32_t* selected; float* out; float* lse_opt;
+    void* workspace; size_t workspace_bytes;
+    int32_t* dev_status;
+} qs_step_params;
+
+qs_status qs_sparse_decode_step(const qs_step_params* params, qs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QUESTSPARSE_H */

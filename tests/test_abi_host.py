@@ -1,0 +1,92 @@
+"""Host-only checks: the C-ABI library builds, loads without a GPU and exports
+every function include/questsparse.h declares; the Python binding rejects
+bad arguments before any CUDA call; host-side helpers behave."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(qs_[a-z_0-9]+)\s*\(", txt))
+    return names
+
+
+@pytest.fixture(scope="module")
+def built_lib():
+    from decode_sparse_attention_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("qs_prefill_metadata", "qs_block_select_paged", "qs_probe_select",
+              "qs_sparse_decode_attn", "qs_sparse_decode_step", "qs_workspace_size",
+              "qs_read_status", "qs_status_string", "qs_version"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    for name in declared_functions():
+        assert hasattr(built_lib, name), name
+
+
+def test_status_strings_and_version(built_lib):
+    built_lib.qs_status_string.restype = ctypes.c_char_p
+    built_lib.qs_status_string.argtypes = [ctypes.c_int32]
+    assert built_lib.qs_status_string(0) == b"ok"
+    assert b"workspace" in built_lib.qs_status_string(5)
+    assert b"block_tables" in built_lib.qs_status_string(101)
+    assert built_lib.qs_version() >= 10000
+
+
+def test_workspace_size_without_gpu(built_lib):
+    from decode_sparse_attention_gb300 import questsparse as qs
+    n = qs.workspace_size(qs.OP_BLOCK_SELECT, 20, 32, 8, 128, 128, 8, 128, 8)
+    assert n >= 20 * 8 * 128 * 4 + 20 * 8 * 4
+    a = qs.workspace_size(qs.OP_SPARSE_ATTN, 20, 32, 8, 128, 128, 8, 128, 8)
+    assert a >= 160 * 4 + 160 * 4 * 130 * 4
+    s = qs.workspace_size(qs.OP_STEP_QUEST, 20, 32, 8, 128, 128, 8, 128, 8)
+    assert s >= n + a
+    with pytest.raises(qs.QuestSparseError):
+        qs.workspace_size(qs.OP_SPARSE_ATTN, 2, 32, 8, 128, 128, 8, 128, 5)   # sel_heads
+
+
+def test_binding_rejects_host_tensors(built_lib):
+    from decode_sparse_attention_gb300 import questsparse as qs
+    q = torch.zeros(1, 4, 64)
+    kc = torch.zeros(2, 16, 2, 64)
+    with pytest.raises(qs.QuestSparseError, match="CUDA"):
+        qs.sparse_decode_attn(q, kc, kc, torch.zeros(1, 2, dtype=torch.int32),
+                              torch.zeros(1, dtype=torch.int32),
+                              torch.zeros(1, 2, 4, dtype=torch.int32))
+
+
+def test_step_params_layout_matches_header():
+    """The ctypes mirror of qs_step_params has the C struct's field order."""
+    from decode_sparse_attention_gb300 import questsparse as qs
+    txt = open(os.path.join(ROOT, "include", "questsparse.h")).read()
+    body = txt[txt.index("typedef struct {\n    int32_t mode;"):txt.index("} qs_step_params;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    c_fields = []
+    for decl in body.replace("typedef struct {", "").split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        # "const int32_t* block_tables" / "int32_t B, H, N" ...
+        parts = decl.split()
+        names = " ".join(parts[1:]) if parts[0] != "const" else " ".join(parts[2:])
+        for nm in names.split(","):
+            c_fields.append(nm.strip().lstrip("*").strip())
+    py_fields = [f[0] for f in qs.StepParams._fields_]
+    assert py_fields == c_fields
