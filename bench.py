@@ -258,11 +258,12 @@ def timed_graph(graph, flush, steps, stream):
     between steps."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    for s, e in evs:
-        flush.zero_()
-        s.record(stream)
-        graph.replay()
-        e.record(stream)
+    with torch.cuda.stream(stream):     # flush, replay and both events on one stream
+        for s, e in evs:
+            flush.zero_()
+            s.record(stream)
+            graph.replay()
+            e.record(stream)
     torch.cuda.synchronize()
     return [s.elapsed_time(e) for s, e in evs]
 
@@ -301,11 +302,12 @@ def run_ours(args, w):
 
     sampler = ClockSampler(local)
     t_end = time.time() + 1.5
-    for _ in range(args.warmup):
-        flush.zero_()
-        g_step.replay()
-    while time.time() < t_end:      # keep the clocks under load for the sampler
-        g_step.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            g_step.replay()
+        while time.time() < t_end:  # keep the clocks under load for the sampler
+            g_step.replay()
     torch.cuda.synchronize()
     barrier()
     durs = timed_graph(g_step, flush, args.steps, stream)

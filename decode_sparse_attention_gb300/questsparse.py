@@ -140,16 +140,24 @@ def workspace_size(op, B, H, N, D, BS, k, max_blocks_per_req, sel_heads):
     return n.value
 
 
-def workspace(nbytes, device, slot="default") -> torch.Tensor:
-    """A zero-filled byte buffer of at least nbytes, cached per (device, slot).
-    The kernels leave it zero-filled after every call."""
+def workspace(nbytes, device, key="default") -> torch.Tensor:
+    """A zero-filled byte buffer of at least nbytes, cached per (device, key).
+
+    A workspace belongs to one set of call sizes: the kernels rearm their
+    arrival counters after every call, but the rest is scratch, so a buffer
+    is only reused by calls whose key (op and sizes) is the same."""
     device = torch.device(device)
-    key = (device.index if device.index is not None else torch.cuda.current_device(), slot)
-    buf = _workspaces.get(key)
-    if buf is None or buf.numel() < nbytes:
+    k = (device.index if device.index is not None else torch.cuda.current_device(), key, nbytes)
+    buf = _workspaces.get(k)
+    if buf is None:
         buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
-        _workspaces[key] = buf
+        _workspaces[k] = buf
     return buf
+
+
+def reset_workspace(buf: torch.Tensor):
+    """Zero a workspace again (needed after a call reported a device error)."""
+    buf.zero_()
 
 
 def read_status(device=None, reset=True) -> int:
@@ -217,7 +225,7 @@ def quest_block_select_paged_in_out_w(query, maxblocks, minblocks, metadata_bloc
         if scores.numel() < B * N * MMBPR * BS:
             raise QuestSparseError("scores must hold [B, N, MMBPR*BS] floats")
     nbytes = workspace_size(OP_BLOCK_SELECT, B, H, N, D, BS, k, MMBPR * BS, N)
-    ws = workspace(nbytes, query.device, "select")
+    ws = workspace(nbytes, query.device, ("select", B, H, N, D, BS, k, MMBPR))
     rc = lib().qs_block_select_paged(_ptr(query), _dt(query), _ptr(maxblocks), _ptr(minblocks),
                                      _dt(maxblocks), _ptr(metadata_block_tables), MMBPR, M,
                                      _ptr(seq_lens), B, H, N, D, BS, k,
@@ -264,7 +272,7 @@ def probe_select(q, k_cache, block_tables, seq_lens, k, n_probe=8, importance=No
     _req(selected, "selected", torch.int32, 3)
     MKBPR = block_tables.shape[1]
     nbytes = workspace_size(OP_PROBE_SELECT, B, H, N, D, BS, k, MKBPR, H)
-    ws = workspace(nbytes, q.device, "probe")
+    ws = workspace(nbytes, q.device, ("probe", B, H, N, D, BS, k, MKBPR))
     rc = lib().qs_probe_select(_ptr(q), _dt(q), _ptr(k_cache), _ptr(k_scale), _dt(k_cache), P_,
                                _ptr(block_tables), MKBPR, _ptr(seq_lens), _ptr(importance),
                                0 if importance is None else importance.shape[1], B, H, N, D, BS,
@@ -297,7 +305,7 @@ def sparse_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, selected, so
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     nbytes = workspace_size(OP_SPARSE_ATTN, B, H, N, D, BS, k, block_tables.shape[1], sel_heads)
-    ws = workspace(nbytes, q.device, "attn")
+    ws = workspace(nbytes, q.device, ("attn", B, H, N, D, BS, k, sel_heads))
     rc = lib().qs_sparse_decode_attn(_ptr(q), _dt(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                      _ptr(v_scale), _dt(k_cache), P_, _ptr(block_tables),
                                      block_tables.shape[1], _ptr(seq_lens), _ptr(selected),

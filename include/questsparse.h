@@ -23,9 +23,13 @@
  *  - All tensor arguments are DEVICE pointers to contiguous row-major memory
  *    owned by the caller.  The library never allocates device memory; the
  *    scratch a call needs is a caller-provided workspace whose size
- *    qs_workspace_size() returns.  A workspace must be zero-filled once before
- *    its first use (and again after a call reported a device-side error); the
- *    calls leave it zero-filled for the next call.
+ *    qs_workspace_size() returns.  A workspace belongs to one operation and
+ *    one set of sizes (B, H, N, D, BS, k, table widths): zero-fill it before
+ *    its first use, and again after a call reported a device-side error.  The
+ *    kernels rearm the arrival counters they keep in it, so consecutive calls
+ *    with the same sizes need no re-zeroing; the rest of it is scratch, so a
+ *    call with other sizes needs a freshly zeroed workspace.  Calls that share
+ *    a workspace must not overlap in time (use one stream).
  *  - Every call enqueues its kernels on `stream` and returns without waiting.
  *    The returned qs_status reports host-side validation and launch errors only.
  *  - Faults found on the device (a table entry out of range, a bad seq_len, an

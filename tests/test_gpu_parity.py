@@ -342,7 +342,7 @@ def test_decode_step_parity(name):
     out = torch.empty((w.B, w.H, w.D), dtype=torch.float32, device=DEV)
     nbytes = qs.step_workspace_bytes(mode, w.B, w.H, w.N, w.D, w.BS, w.k,
                                      MMBPR=g["meta_block_tables"].shape[1], MKBPR=x["MKBPR"])
-    ws = qs.workspace(nbytes, DEV, "step")
+    ws = qs.workspace(nbytes, DEV, ("step", name))
     p = qs.make_step_params(mode, g["q"], g["k_cache"], g["v_cache"], g["block_tables"],
                             g["seq_lens"], w.k, sel, out, ws, maxblocks=g.get("maxblocks"),
                             minblocks=g.get("minblocks"),
