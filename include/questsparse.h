@@ -200,6 +200,34 @@ qs_status qs_sparse_decode_attn(const void* q, qs_dtype q_dtype, const void* k_c
                                 float* lse_opt, void* workspace, size_t workspace_bytes,
                                 int32_t* dev_status, qs_stream_t stream);
 
+/*
+ * qs_sparse_decode_attn without a workspace, for callers that cannot allocate
+ * device memory (a decode loop that forbids allocations once it is running, a
+ * plugin that is handed only input and output pointers).  The pages describe
+ * nothing like it; it exists for those callers.  Same arguments, layouts,
+ * results and device-side error reporting as qs_sparse_decode_attn.
+ *  - Scratch comes from one fixed 4 MiB array in device memory that the
+ *    library holds on every GPU that loads it, until the process exits.  Sizes
+ *    that need more (attention workspace above 4 MiB, i.e. more than about 990
+ *    (request, KV head) units at H/N = 4, D = 128) return QS_EWORKSPACE.
+ *  - The first call on a device looks up the array's device address; make
+ *    that first call outside of any stream capture.
+ *  - Every call clears the part of the array that must start at zero (an
+ *    async memset on `stream`), then runs the attention.  All calls on a
+ *    device share the array: calls that overlap on the GPU race -- keep them
+ *    on one stream.
+ *  - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ */
+qs_status qs_sparse_decode_attn_noalloc(const void* q, qs_dtype q_dtype, const void* k_cache,
+                                        const void* v_cache, const float* k_scale,
+                                        const float* v_scale, qs_dtype kv_dtype,
+                                        int32_t num_kv_blocks, const int32_t* block_tables,
+                                        int32_t MKBPR, const int32_t* seq_lens,
+                                        const int32_t* selected, int32_t sel_heads, int32_t k,
+                                        float softmax_scale, int32_t B, int32_t H, int32_t N,
+                                        int32_t D, int32_t BS, float* out, float* lse_opt,
+                                        int32_t* dev_status, qs_stream_t stream);
+
 /* One decode step: a selector followed by the attention, enqueued back to back
  * on one stream (the attention is launched as a programmatic dependent of the
  * selector).  Quest mode reads maxblocks/minblocks/meta tables and writes
