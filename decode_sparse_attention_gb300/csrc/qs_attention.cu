@@ -8,22 +8,26 @@
 //  * Work = (unit, selected block, sub-tile) tiles; a unit is (request, KV
 //    head) when the selection is per KV head -- all H/N query heads of the
 //    group share each K/V tile, read once -- or (request, query head).
-//  * Persistent grid of one CTA per SM; CTA c owns a contiguous range of
+//  * Persistent grid of about one CTA per SM; CTA c owns a contiguous range of
 //    tiles (stream-K split), so every SM streams the same number of tiles.
-//  * One producer warp gathers the tiles with 2-D TMA loads (tensor maps over
-//    the whole paged pool; box = one head's [rows x D] slice of one block)
-//    into a multi-stage shared-memory ring guarded by mbarriers; the unit's
-//    query rows come in with a 1-D bulk copy.  Eight consumer warps compute.
-//  * Each consumer warp keeps its own online-softmax state (running max, sum,
-//    accumulator) over its rows of every tile, so tiles need no CTA-wide
-//    barrier; warps are merged at the end of a unit.  Q.K uses 8 lanes per
-//    token and packed fp32x2 FMAs with a transposing shuffle reduction; P.V
-//    gives each lane D/32 output channels.
+//  * A prologue stages the CTA's tile list (selected block -> physical rows,
+//    valid rows, unit) and the queries of its units in shared memory.
+//  * Every warp owns a fixed slice of rows of each tile and streams exactly
+//    those rows with 16-byte cp.async copies into its own multi-stage ring,
+//    several tiles ahead, so the warps never wait on one another between
+//    tiles.  (A head slice of a paged block is rows of D elements 2 KB apart;
+//    gathered with 2-D TMA boxes or per-row bulk copies, the copy engine's
+//    request rate capped a whole SM near 32 GB/s on GB300, so the gather
+//    uses the load/store path, which all 256 threads feed in parallel.)
+//  * Each warp keeps its own online-softmax state (running max, sum,
+//    accumulator) over its rows; warps are merged at the end of a unit.  Q.K
+//    uses 8 lanes per token and packed fp32x2 FMAs with a transposing shuffle
+//    reduction; P.V gives each lane D/32 output channels.
 //  * A unit split across CTAs is merged on the device: each CTA writes a
 //    (max, sum, acc) partial; the last to arrive (atomic counter, no spin)
 //    combines them and rearms the counter.
-//  * Launched as a programmatic dependent of the selector: barrier set-up and
-//    tensor-map prefetch overlap the selector's tail.
+//  * Launched as a programmatic dependent of the selector: block-table and
+//    query prefetches overlap the selector's tail.
 #include <cmath>
 
 #include "qs_common.cuh"
@@ -31,18 +35,25 @@
 namespace qs {
 namespace {
 
-constexpr int kNW = 8;                      // consumer warps
-constexpr int kThreadsAttn = (kNW + 1) * 32;
+constexpr int kMaxWarps = 16;
+constexpr int kRPW = 8;                  // rows of a tile each warp owns
+constexpr int kQSlots = 8;               // units a CTA's tile range may touch
+constexpr int kMaxTilesPerCta = 512;
+constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 225 * 1024;
 
 struct AttnArgs {
     const uint8_t* q;
     int q_dt, q_es;
+    const uint8_t* kc;
+    const uint8_t* vc;
+    const float* ks;
+    const float* vs;
     const int32_t* bt;
     int MKBPR;
     const int32_t* seq_lens;
     const int32_t* sel;
-    int sel_heads, k, num_kv_blocks, B, H, N, BS, TR, split, S;
+    int sel_heads, k, num_kv_blocks, B, H, N, BS, TR, split, S, NW, rpw;
     float scale_log2;
     float* out;
     float* lse;
@@ -51,22 +62,49 @@ struct AttnArgs {
     long long T;
     int tpc;
     int32_t* dev_status;
-    // dynamic shared memory layout (bytes from the 1024-aligned base)
-    uint32_t off_v, off_q, off_sc, off_info, off_bar, off_p, off_alpha, off_merge;
-    uint32_t tile_bytes, q_slot, sc_tile, sc_bytes;
+    // dynamic shared memory layout (bytes)
+    uint32_t off_q, off_stage, off_p, off_alpha, off_ml;
+    uint32_t stage_bytes;    // one warp's slot of one stage
+    uint32_t rows_bytes;     // rpw rows of one head: rpw * D * elem bytes
 };
 
 struct TileInfo {
-    int unit;
-    int rows;
-    int new_unit;
-    int pad;
+    int row0;    // first pool row of the tile: block * BS + sub-tile * TR
+    int rows;    // valid rows in the tile (0: nothing to do)
+    int unit;    // unit index relative to the CTA's first unit
+    int flags;   // kFirst | kLast | (KV head << 8); precomputed so that the
+                 // tile loop does no integer division
 };
+constexpr int kFirst = 1, kLast = 2;
 
 template <Dt KT> struct KvTraits {
     static constexpr int es = DtInfo<KT>::bytes;
     static constexpr int epc = 16 / es;  // elements per 16-byte chunk
 };
+
+QS_DEVINL void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+QS_DEVINL void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+QS_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most n of this thread's copy groups are still pending.
+QS_DEVINL void cp_async_wait(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    }
+}
+QS_DEVINL void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 // ---- Q.K partial over one 16-byte chunk of a K row, G heads ---------------
 
@@ -133,23 +171,12 @@ template <int G> QS_DEVINL bool rep_lane(int g) {
     return G == 4 ? !(g & 1) : G == 2 ? !(g & 3) : g == 0;
 }
 
-QS_DEVINL void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
 QS_DEVINL float sext8(uint32_t w, int i) {
     return static_cast<float>(static_cast<int32_t>(w << (24 - 8 * i)) >> 24);
 }
 
 template <Dt KT, int D, int G>
-__global__ void __launch_bounds__(kThreadsAttn, 1)
-sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                   const __grid_constant__ CUtensorMap ksmap,
-                   const __grid_constant__ CUtensorMap vsmap, const AttnArgs a) {
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const AttnArgs a) {
     constexpr bool kInt8 = KT == Dt::I8;
     constexpr int ES = KvTraits<KT>::es;
     constexpr int EPC = KvTraits<KT>::epc;
@@ -159,135 +186,139 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     static_assert(CR % 8 == 0 && CPL >= 1, "K row must split over 8 lanes");
     static_assert(EPL % 2 == 0, "P.V uses fp32 pairs");
 
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
-
-    const int S = a.S;
-    uint8_t* kt = smem;
-    uint8_t* vt = smem + a.off_v;
-    uint8_t* qsl = smem + a.off_q;
-    uint8_t* sct = smem + a.off_sc;
-    TileInfo* info = reinterpret_cast<TileInfo*>(smem + a.off_info);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
-    uint64_t* empty = full + S;
+    TileInfo* info = reinterpret_cast<TileInfo*>(smem);
+    uint8_t* qslots = smem + a.off_q;
+    uint8_t* stages = smem + a.off_stage;
     unsigned long long* pbuf = reinterpret_cast<unsigned long long*>(smem + a.off_p);
     float* alpha_s = reinterpret_cast<float*>(smem + a.off_alpha);
-    float* merge = reinterpret_cast<float*>(smem + a.off_merge);
+    float* ml = reinterpret_cast<float*>(smem + a.off_ml);
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, nthreads = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int S = a.S;
+    constexpr int rpw = kRPW;
+    constexpr int qpw = kRPW / 4;         // token quads per warp and tile
     const long long tpu = static_cast<long long>(a.k) * a.split;  // tiles per unit
     const long long t0 = static_cast<long long>(blockIdx.x) * a.tpc;
     const long long t1 = min(a.T, t0 + a.tpc);
+    const int n = static_cast<int>(t1 - t0);
+    const long long u_first = t0 / tpu;
+    const int n_units = static_cast<int>((t1 - 1) / tpu - u_first + 1);
     const int G_per_kv = a.H / a.N;
+    const size_t qrow_bytes = static_cast<size_t>(G) * D * a.q_es;   // one unit's q rows
+    constexpr int kQSlotFloats = G * D;                                  // fp32 copy in smem
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kNW);
-        }
-        fence_mbar_init();
+    // ---- prologue, part 1 (overlaps the selector): warm L2 with the block
+    // tables and queries of this CTA's requests
+    for (int us = 0; us < n_units; ++us) {
+        const long long u = u_first + us;
+        const int b = static_cast<int>(u / a.sel_heads), s = static_cast<int>(u % a.sel_heads);
+        const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
+        const int32_t* btr = a.bt + static_cast<size_t>(b) * a.MKBPR;
+        for (int o = tid * 32; o < a.MKBPR; o += nthreads * 32) prefetch_l2(btr + o);
+        const uint8_t* qr = a.q + (static_cast<size_t>(b) * a.H + h0) * D * a.q_es;
+        for (size_t o = static_cast<size_t>(tid) * 128; o < qrow_bytes;
+             o += static_cast<size_t>(nthreads) * 128)
+            prefetch_l2(qr + o);
     }
-    if (warp == kNW && lane == 0) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
-        if constexpr (kInt8) {
-            prefetch_tensormap(&ksmap);
-            prefetch_tensormap(&vsmap);
-        }
-    }
-    __syncthreads();
     pdl_wait();  // the selection is written by the preceding kernel
 
-    if (warp == kNW) {
-        // ------------------------------------------------------------ producer
-        bool timed_out = false;
-        for (long long tb = t0; tb < t1 && !timed_out; tb += 32) {
-            const long long t = tb + lane;
-            int u = 0, rows = 0, p = 0, nu = 0, x = 0, y = 0;
-            size_t qoff = 0;
-            if (t < t1) {
-                u = static_cast<int>(t / tpu);
-                const int i2 = static_cast<int>(t % tpu);
-                const int sidx = i2 / a.split, sp = i2 % a.split;
-                const int b = u / a.sel_heads, s = u % a.sel_heads;
-                const int n = a.sel_heads == a.N ? s : s / G_per_kv;
-                const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
-                nu = (t == t0) || (i2 == 0);
-                qoff = (static_cast<size_t>(b) * a.H + h0) * D * a.q_es;
-                const int j = a.sel[static_cast<size_t>(u) * a.k + sidx];
-                const int L = a.seq_lens[b];
-                if (j >= 0) {
-                    if (L < 0 || L > a.MKBPR * a.BS) {
-                        set_status(a.dev_status, QS_DEV_ESEQ_LEN);
-                    } else if (j >= (L + a.BS - 1) / a.BS) {
-                        set_status(a.dev_status, QS_DEV_ESELECTED);
-                    } else {
-                        p = a.bt[static_cast<size_t>(b) * a.MKBPR + j];
-                        if (p < 0 || p >= a.num_kv_blocks) {
-                            set_status(a.dev_status, QS_DEV_EBLOCK_TABLE);
-                        } else {
-                            rows = min(a.TR, max(0, L - j * a.BS - sp * a.TR));
-                            x = n * D;
-                            y = p * a.BS + sp * a.TR;
-                        }
-                    }
+    // ---- prologue, part 2: tile list and the units' queries
+    for (int i = tid; i < n; i += nthreads) {
+        const long long t = t0 + i;
+        const long long u = t / tpu;
+        const int i2 = static_cast<int>(t % tpu);
+        const int sidx = i2 / a.split, sp = i2 % a.split;
+        const int b = static_cast<int>(u / a.sel_heads);
+        const int j = a.sel[u * a.k + sidx];
+        const int L = a.seq_lens[b];
+        const int s_row = static_cast<int>(u % a.sel_heads);
+        const int nkv = a.sel_heads == a.N ? s_row : s_row / G_per_kv;
+        const int flags = ((i == 0 || i2 == 0) ? kFirst : 0) |
+                          ((i == n - 1 || i2 == tpu - 1) ? kLast : 0) | (nkv << 8);
+        TileInfo ti{0, 0, static_cast<int>(u - u_first), flags};
+        if (j >= 0) {
+            if (L < 0 || L > a.MKBPR * a.BS) {
+                set_status(a.dev_status, QS_DEV_ESEQ_LEN);
+            } else if (j >= (L + a.BS - 1) / a.BS) {
+                set_status(a.dev_status, QS_DEV_ESELECTED);
+            } else {
+                const int p = a.bt[static_cast<size_t>(b) * a.MKBPR + j];
+                if (p < 0 || p >= a.num_kv_blocks) {
+                    set_status(a.dev_status, QS_DEV_EBLOCK_TABLE);
+                } else {
+                    ti.rows = min(a.TR, max(0, L - j * a.BS - sp * a.TR));
+                    ti.row0 = p * a.BS + sp * a.TR;
                 }
             }
-            const int cnt = static_cast<int>(min(32LL, t1 - tb));
-            bool stop = false;
-            for (int ii = 0; ii < cnt && !stop; ++ii) {
-                const int rows_i = __shfl_sync(0xffffffffu, rows, ii);
-                const int u_i = __shfl_sync(0xffffffffu, u, ii);
-                const int nu_i = __shfl_sync(0xffffffffu, nu, ii);
-                const int x_i = __shfl_sync(0xffffffffu, x, ii);
-                const int y_i = __shfl_sync(0xffffffffu, y, ii);
-                const unsigned long long qo_i = __shfl_sync(0xffffffffu, static_cast<unsigned long long>(qoff), ii);
-                const long long i = tb + ii - t0;
-                const int st = static_cast<int>(i % S);
-                int ok = 1;
-                if (lane == 0) {
-                    const uint32_t par = static_cast<uint32_t>((i / S) & 1) ^ 1u;
-                    ok = mbar_wait(&empty[st], par) ? 1 : 0;
-                    if (!ok) set_status(a.dev_status, QS_DEV_ETIMEOUT);
-                }
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {        // warp-uniform exit
-                    stop = true;
-                    break;
-                }
-                if (lane == 0) {
-                    info[st] = TileInfo{u_i, rows_i, nu_i, 0};
-                    uint32_t bytes = 0;
-                    if (rows_i > 0) bytes += 2 * a.tile_bytes + (kInt8 ? 2 * a.sc_bytes : 0);
-                    const uint32_t qbytes = static_cast<uint32_t>(G * D * a.q_es);
-                    if (nu_i) bytes += qbytes;
-                    mbar_arrive_expect_tx(&full[st], bytes);
-                    if (rows_i > 0) {
-                        tma_load_2d(kt + static_cast<size_t>(st) * a.tile_bytes, &kmap, x_i, y_i, &full[st]);
-                        tma_load_2d(vt + static_cast<size_t>(st) * a.tile_bytes, &vmap, x_i, y_i, &full[st]);
-                        if constexpr (kInt8) {
-                            tma_load_2d(sct + static_cast<size_t>(st) * 2 * a.sc_tile, &ksmap, 0, y_i, &full[st]);
-                            tma_load_2d(sct + static_cast<size_t>(st) * 2 * a.sc_tile + a.sc_tile, &vsmap, 0, y_i,
-                                        &full[st]);
-                        }
-                    }
-                    if (nu_i) bulk_copy_g2s(qsl + static_cast<size_t>(st) * a.q_slot, a.q + qo_i, qbytes, &full[st]);
-                }
-                __syncwarp();
-            }
-            timed_out = stop;
         }
-        return;
+        info[i] = ti;
     }
+    {
+        // query rows of the units in range, converted once to fp32
+        float* qf = reinterpret_cast<float*>(qslots);
+        for (int e = tid; e < n_units * kQSlotFloats; e += nthreads) {
+            const int us = e / kQSlotFloats, hd = e % kQSlotFloats;
+            const long long u = u_first + us;
+            const int b = static_cast<int>(u / a.sel_heads), s = static_cast<int>(u % a.sel_heads);
+            const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
+            qf[e] = load_q(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + h0) * D + hd);
+        }
+    }
+    // zero the rings once: rows a warp does not load keep finite contents, so
+    // the unrolled row loops below never read non-finite leftovers
+    for (size_t o = static_cast<size_t>(tid) * 16; o < static_cast<size_t>(a.NW) * S * a.stage_bytes;
+         o += static_cast<size_t>(nthreads) * 16)
+        *reinterpret_cast<uint4*>(stages + o) = make_uint4(0, 0, 0, 0);
+    __syncthreads();
 
-    // ---------------------------------------------------------------- consumers
-    const int tq = lane >> 3, g = lane & 7;
-    const int TR = a.TR;
-    const int nwa = min(kNW, TR / 4);         // warps with rows in a tile
-    const int rpw = TR / nwa;                 // rows per active warp
-    const int qpw = rpw / 4;                  // quads per warp
-    const bool wact = warp < nwa;
+    // ---- per-warp row streams
     const int r0 = warp * rpw;
+    uint8_t* mine = stages + static_cast<size_t>(warp) * S * a.stage_bytes;
+    const size_t pool_row = static_cast<size_t>(a.N) * D * ES;   // bytes between tokens
+
+    // lane -> (row within a copy step, 16-byte chunk) of the warp's rows
+    constexpr int kRowsPerCopy = CR >= 32 ? 1 : 32 / CR;          // rows one warp copy covers
+    constexpr int kCopies = (rpw * CR + 31) / 32;                   // copy steps per array
+    const int c_row = CR >= 32 ? 0 : lane / CR;
+    const int c_chunk = CR >= 32 ? lane : lane % CR;
+    auto issue = [&](int i, int st) {
+        if (i < n) {
+            const TileInfo ti = info[i];
+            const int rw = min(rpw, ti.rows - r0);
+            if (rw > 0) {
+                const int nkv = ti.flags >> 8;
+                uint8_t* dst = mine + static_cast<size_t>(st) * a.stage_bytes +
+                               c_row * D * ES + c_chunk * 16;
+                const size_t first = (static_cast<size_t>(ti.row0) + r0 + c_row) * pool_row +
+                                     static_cast<size_t>(nkv) * D * ES + c_chunk * 16;
+                const uint8_t* ksrc = a.kc + first;
+                const uint8_t* vsrc = a.vc + first;
+#pragma unroll
+                for (int j = 0; j < kCopies; ++j) {
+                    if (c_row + j * kRowsPerCopy < rw && (CR >= 32 || j * 32 + lane < rpw * CR)) {
+                        const size_t so = static_cast<size_t>(j * kRowsPerCopy) * pool_row;
+                        const int d_off = j * kRowsPerCopy * D * ES;
+                        cp_async16(dst + d_off, ksrc + so);
+                        cp_async16(dst + a.rows_bytes + d_off, vsrc + so);
+                    }
+                }
+                if constexpr (kInt8) {
+                    uint8_t* sdst = mine + static_cast<size_t>(st) * a.stage_bytes + 2 * a.rows_bytes;
+                    if (lane < rw) {
+                        const size_t si = (static_cast<size_t>(ti.row0) + r0 + lane) * a.N + nkv;
+                        cp_async4(sdst + lane * 4, a.ks + si);
+                        cp_async4(sdst + rpw * 4 + lane * 4, a.vs + si);
+                    }
+                }
+            }
+        }
+        cp_async_commit();
+    };
+
+    const int tq = lane >> 3, g = lane & 7;
     const int hl = head_of_lane<G>(g);
     const bool rep = rep_lane<G>(g);
 
@@ -304,29 +335,28 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     }
     unsigned long long* pw = pbuf + static_cast<size_t>(warp) * rpw * G;
     float* aw = alpha_s + warp * G;
-    const int ct = threadIdx.x;               // consumer thread id, < kNW*32
 
-    bool failed = false;
-    for (long long t = t0; t < t1; ++t) {
-        const long long i = t - t0;
-        const int st = static_cast<int>(i % S);
-        const uint32_t par = static_cast<uint32_t>((i / S) & 1);
-        if (!mbar_wait(&full[st], par)) {
-            set_status(a.dev_status, QS_DEV_ETIMEOUT);
-            failed = true;
-            break;
-        }
-        const TileInfo ti = info[st];
-        if (ti.new_unit) {
+    for (int i = 0; i < S - 1; ++i) issue(i, i);
+    int st_cur = 0, st_next = S - 1;            // ring slots of tiles i and i+S-1
+    for (int i = 0; i < n; ++i) {
+        issue(i + S - 1, st_next);
+        st_next = st_next + 1 == S ? 0 : st_next + 1;
+        cp_async_wait(S - 1);
+        __syncwarp();
+        const TileInfo ti = info[i];
+        const int st = st_cur;
+        st_cur = st_cur + 1 == S ? 0 : st_cur + 1;
+        uint8_t* cur = mine + static_cast<size_t>(st) * a.stage_bytes;
+        if (ti.flags & kFirst) {
             // query rows of the unit, fp32 (and int8 quantised for int8 caches)
-            const uint8_t* qs = qsl + static_cast<size_t>(st) * a.q_slot;
+            const float* qs = reinterpret_cast<const float*>(qslots) + static_cast<size_t>(ti.unit) * kQSlotFloats;
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 float s_q = 0.f;
                 if constexpr (kInt8) {
                     float amax = 0.f;
-                    for (int d = lane; d < D; d += 32)
-                        amax = fmaxf(amax, fabsf(load_q(qs, a.q_dt, static_cast<size_t>(h) * D + d)));
+#pragma unroll
+                    for (int d = lane; d < D; d += 32) amax = fmaxf(amax, fabsf(qs[h * D + d]));
 #pragma unroll
                     for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
                     s_q = amax == 0.f ? 0.f : __fdiv_rn(amax, 127.f);
@@ -337,7 +367,10 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                     const int d0 = (g + 8 * c) * EPC;
                     float qv[EPC];
 #pragma unroll
-                    for (int e = 0; e < EPC; ++e) qv[e] = load_q(qs, a.q_dt, static_cast<size_t>(h) * D + d0 + e);
+                    for (int e = 0; e < EPC; e += 4) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(qs + h * D + d0 + e);
+                        qv[e] = v4.x; qv[e + 1] = v4.y; qv[e + 2] = v4.z; qv[e + 3] = v4.w;
+                    }
                     if constexpr (kInt8) {
 #pragma unroll
                         for (int w4 = 0; w4 < 4; ++w4) {
@@ -358,20 +391,18 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 }
             }
         }
-        if (wact && ti.rows > 0) {
-            const int rows = ti.rows;
-            const uint8_t* ktile = kt + static_cast<size_t>(st) * a.tile_bytes;
-            const uint8_t* vtile = vt + static_cast<size_t>(st) * a.tile_bytes;
-            const float* kst = reinterpret_cast<const float*>(sct + static_cast<size_t>(st) * 2 * a.sc_tile);
-            const float* vst = reinterpret_cast<const float*>(sct + static_cast<size_t>(st) * 2 * a.sc_tile + a.sc_tile);
-            const int n_kv = (ti.unit % a.sel_heads) / (a.sel_heads == a.N ? 1 : G_per_kv);
+        const int rw = min(rpw, ti.rows - r0);
+        if (rw > 0) {
+            const uint8_t* ktile = cur;
+            const uint8_t* vtile = cur + a.rows_bytes;
+            const float* kst = reinterpret_cast<const float*>(cur + 2 * a.rows_bytes);
+            const float* vst = kst + rpw;
             // ---- Q.K for the warp's rows
-            float x[8];
+            float x[qpw];
 #pragma unroll
-            for (int qi = 0; qi < 8; ++qi) {
-                x[qi] = -INFINITY;
-                if (qi < qpw) {
-                    const int row = r0 + 4 * qi + tq;
+            for (int qi = 0; qi < qpw; ++qi) {
+                {
+                    const int row = 4 * qi + tq;
                     const uint8_t* krow = ktile + static_cast<size_t>(row) * D * ES;
                     float s;
                     if constexpr (kInt8) {
@@ -389,7 +420,7 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                                 for (int e = 0; e < 4; ++e) iacc[h] = __dp4a(q8w[c][h][e], w[e], iacc[h]);
                         }
                         const int tot = reduce8<G, int>(iacc, g);
-                        const float sk = kst[row * a.N + n_kv];
+                        const float sk = row < rw ? kst[row] : 0.f;
                         s = __fmul_rn(__fmul_rn(sq[hl], sk), static_cast<float>(tot)) * a.scale_log2;
                     } else {
                         unsigned long long pacc[G];
@@ -408,25 +439,23 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                         }
                         s = reduce8<G, float>(hs, g) * a.scale_log2;
                     }
-                    x[qi] = row < rows ? s : -INFINITY;
+                    x[qi] = row < rw ? s : -INFINITY;
                 }
             }
             // ---- online softmax update (per warp, per head)
             float mx = x[0];
 #pragma unroll
-            for (int qi = 1; qi < 8; ++qi) mx = fmaxf(mx, x[qi]);
+            for (int qi = 1; qi < qpw; ++qi) mx = fmaxf(mx, x[qi]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float m_new = fmaxf(m_run, mx);
             const float alpha = m_new == -INFINITY ? 1.f : exp2_approx(m_run - m_new);
             float lsum = 0.f;
 #pragma unroll
-            for (int qi = 0; qi < 8; ++qi) {
-                if (qi < qpw) {
-                    const float p = m_new == -INFINITY ? 0.f : exp2_approx(x[qi] - m_new);
-                    lsum += p;
-                    if (rep) pw[(4 * qi + tq) * G + hl] = pack2(p, p);
-                }
+            for (int qi = 0; qi < qpw; ++qi) {
+                const float p = m_new == -INFINITY ? 0.f : exp2_approx(x[qi] - m_new);
+                lsum += p;
+                if (rep) pw[(4 * qi + tq) * G + hl] = pack2(p, p);
             }
             lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
             lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
@@ -435,29 +464,28 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             if (rep && tq == 0) aw[hl] = alpha;
             __syncwarp();
             // ---- P.V for the warp's rows
-            float al[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) al[h] = aw[h];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const unsigned long long a2 = pack2(al[h], al[h]);
+                const float al = aw[h];
+                const unsigned long long a2 = pack2(al, al);
 #pragma unroll
                 for (int e = 0; e < EPL / 2; ++e) acc[h][e] = mul2(acc[h][e], a2);
             }
-            const int rmax = min(rpw, rows - r0);
-            for (int r = 0; r < rmax; ++r) {
-                const int row = r0 + r;
+            // every row of the warp's slice; rows past rw have p = 0 and
+            // finite (zeroed or earlier) data in the ring
+#pragma unroll
+            for (int r = 0; r < rpw; ++r) {
                 float v[EPL];
                 if constexpr (KT == Dt::F32) {
-                    const float* vr = reinterpret_cast<const float*>(vtile + static_cast<size_t>(row) * D * 4) + lane * EPL;
+                    const float* vr = reinterpret_cast<const float*>(vtile + static_cast<size_t>(r) * D * 4) + lane * EPL;
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) v[e] = vr[e];
                 } else if constexpr (kInt8) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vtile + static_cast<size_t>(row) * D + lane * EPL);
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vtile + static_cast<size_t>(r) * D + lane * EPL);
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) v[e] = sext8(w, e);
                 } else {
-                    const uint32_t* vr = reinterpret_cast<const uint32_t*>(vtile + static_cast<size_t>(row) * D * 2 + lane * EPL * 2);
+                    const uint32_t* vr = reinterpret_cast<const uint32_t*>(vtile + static_cast<size_t>(r) * D * 2 + lane * EPL * 2);
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e) {
                         const float2 f = pair_to_float2<KT>(vr[e]);
@@ -466,61 +494,59 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                     }
                 }
                 const unsigned long long* prow = pw + r * G;
-                float vs = 1.f;
-                if constexpr (kInt8) vs = vst[row * a.N + n_kv];
+                float vsc = 1.f;
+                if constexpr (kInt8) vsc = vst[r];
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     unsigned long long p2 = prow[h];
                     if constexpr (kInt8) {
                         const float2 pf = unpack2(p2);
-                        p2 = pack2(pf.x * vs, pf.y * vs);
+                        p2 = pack2(pf.x * vsc, pf.y * vsc);
                     }
 #pragma unroll
                     for (int e = 0; e < EPL / 2; ++e) acc[h][e] = fma2(p2, pack2(v[2 * e], v[2 * e + 1]), acc[h][e]);
                 }
             }
-            __syncwarp();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
 
         // ---- end of a unit within this CTA: merge warps, write output/partial
-        if (t + 1 == t1 || (t + 1) % tpu == 0) {
-            const int u = static_cast<int>(t / tpu);
-            float* mw = merge;                                   // [kNW][G] max
-            float* lw = merge + kNW * G;                         // [kNW][G] sum
-            float* accw = merge + 2 * kNW * G;                   // [kNW][G][D]
+        if (ti.flags & kLast) {
+            const long long t = t0 + i;
+            const int u = static_cast<int>(u_first + ti.unit);
+            float* accw = reinterpret_cast<float*>(cur);     // this warp's consumed stage slot
             if (rep && tq == 0) {
-                mw[warp * G + hl] = m_run;
-                lw[warp * G + hl] = l_run;
+                ml[warp * 2 * G + hl] = m_run;
+                ml[warp * 2 * G + G + hl] = l_run;
             }
 #pragma unroll
             for (int h = 0; h < G; ++h)
 #pragma unroll
                 for (int e = 0; e < EPL / 2; ++e) {
                     const float2 f = unpack2(acc[h][e]);
-                    accw[(warp * G + h) * D + lane * EPL + 2 * e] = f.x;
-                    accw[(warp * G + h) * D + lane * EPL + 2 * e + 1] = f.y;
+                    accw[h * D + lane * EPL + 2 * e] = f.x;
+                    accw[h * D + lane * EPL + 2 * e + 1] = f.y;
                 }
-            named_bar_sync(1, kNW * 32);
+            __syncthreads();
             const long long ut0 = static_cast<long long>(u) * tpu, ut1 = ut0 + tpu;
             const bool owned = ut0 >= t0 && ut1 <= t1;
             const int b = u / a.sel_heads, s = u % a.sel_heads;
             const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
             const int c = blockIdx.x;
             float* slot = a.partial + static_cast<size_t>(c + u) * G * (D + 2);
-            for (int idx = ct; idx < G * D; idx += kNW * 32) {
+            const int NW = a.NW;
+            for (int idx = tid; idx < G * D; idx += nthreads) {
                 const int h = idx / D, d = idx % D;
                 float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kNW; ++w) M = fmaxf(M, mw[w * G + h]);
+                for (int w = 0; w < NW; ++w) M = fmaxf(M, ml[w * 2 * G + h]);
                 float Ls = 0.f, A = 0.f;
                 if (M != -INFINITY) {
-#pragma unroll
-                    for (int w = 0; w < kNW; ++w) {
-                        const float f = exp2_approx(mw[w * G + h] - M);
-                        Ls += lw[w * G + h] * f;
-                        A += accw[(w * G + h) * D + d] * f;
+                    for (int w = 0; w < NW; ++w) {
+                        const float f = exp2_approx(ml[w * 2 * G + h] - M);
+                        const float* aw2 = reinterpret_cast<const float*>(
+                            stages + (static_cast<size_t>(w) * S + st) * a.stage_bytes);
+                        Ls += ml[w * 2 * G + G + h] * f;
+                        A += aw2[h * D + d] * f;
                     }
                 }
                 if (owned) {
@@ -538,19 +564,19 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             }
             if (!owned) {
                 __threadfence();
-                named_bar_sync(1, kNW * 32);
+                __syncthreads();
                 const int c_first = static_cast<int>(ut0 / a.tpc);
                 const int c_last = static_cast<int>((ut1 - 1) / a.tpc);
-                if (ct == 0) {
+                if (tid == 0) {
                     const uint32_t prev = atomicAdd(&a.counters[u], 1u);
                     const bool last = prev == static_cast<uint32_t>(c_last - c_first);
                     if (last) a.counters[u] = 0;
                     s_last = last;
                 }
-                named_bar_sync(1, kNW * 32);
+                __syncthreads();
                 if (s_last) {
                     __threadfence();
-                    for (int idx = ct; idx < G * D; idx += kNW * 32) {
+                    for (int idx = tid; idx < G * D; idx += nthreads) {
                         const int h = idx / D, d = idx % D;
                         float M = -INFINITY;
                         for (int cc = c_first; cc <= c_last; ++cc)
@@ -578,115 +604,88 @@ sparse_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             for (int h = 0; h < G; ++h)
 #pragma unroll
                 for (int e = 0; e < EPL / 2; ++e) acc[h][e] = 0ull;
-            named_bar_sync(1, kNW * 32);
+            __syncthreads();
         }
     }
-    (void)failed;
-}
-
-}  // namespace
-}  // namespace qs
-
-namespace qs {
-namespace {
-
-constexpr int kMaxGrid = 1024;
-
-bool tmap_dtype(int es, CUtensorMapDataType* dt) {
-    switch (es) {
-        case 1: *dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; return true;
-        case 2: *dt = CU_TENSOR_MAP_DATA_TYPE_UINT16; return true;
-        case 4: *dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; return true;
-        default: return false;
-    }
+    cp_async_wait(0);
 }
 
 struct AttnPlan {
-    int TR, split, S, grid;
+    int grid, threads;
     size_t smem;
 };
 
-// Tile rows, split and ring depth: the smallest per-CTA critical path
+// Tile rows, split, warps and ring depth: the smallest per-CTA critical path
 // (tiles x rows, plus a per-tile overhead) over the admissible sub-tilings.
-bool plan_attention(int BS, int D, int G, int es, int q_es, int N, bool int8, long long units,
-                    int k, AttnArgs* a, AttnPlan* pl) {
+bool plan_attention(int BS, int D, int G, int es, int q_es, bool int8, long long units, int k,
+                    AttnArgs* a, AttnPlan* pl) {
     const int nsm = num_sms();
     long long best_cost = -1;
-    for (int split = 1; split <= 8; split *= 2) {
+    int best_split = 0;
+    for (int split = 1; split <= 16; split *= 2) {
         if (BS % split) break;
         const int TR = BS / split;
-        if (TR < 16 || TR % 16 || TR > 256) continue;
+        if (TR < 16 || TR % 16 || TR > kMaxWarps * kRPW) continue;
         const long long T = units * k * split;
         const long long tpc = (T + nsm - 1) / nsm;
         const long long cost = tpc * (TR + 24);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
-            pl->TR = TR;
-            pl->split = split;
+            best_split = split;
         }
     }
     if (best_cost < 0) return false;
-    const int TR = pl->TR;
-    const int nwa = TR / 4 < kNW ? TR / 4 : kNW;
-    const int rpw = TR / nwa;
-    const uint32_t tile_bytes = static_cast<uint32_t>(TR) * D * es;
-    const uint32_t q_slot = static_cast<uint32_t>(align_up(static_cast<size_t>(G) * D * q_es, 128));
-    const uint32_t sc_tile = int8 ? static_cast<uint32_t>(align_up(static_cast<size_t>(TR) * N * 4, 128)) : 0;
-    const size_t per_stage = 2 * static_cast<size_t>(tile_bytes) + q_slot + 2 * sc_tile + 16 + 16;
-    const size_t fixed = 1024 /* alignment slack */ + static_cast<size_t>(kNW) * rpw * G * 8 +
-                         kNW * G * 4 + (2 * kNW * G + static_cast<size_t>(kNW) * G * D) * 4 + 256;
-    long long S = (static_cast<long long>(kSmemBudget) - static_cast<long long>(fixed)) /
-                  static_cast<long long>(per_stage);
-    if (S > 8) S = 8;
-    if (S < 2) return false;
-    pl->S = static_cast<int>(S);
-    size_t off = 0;
-    off += S * tile_bytes;
-    a->off_v = static_cast<uint32_t>(off);
-    off += S * tile_bytes;
+    const int split = best_split, TR = BS / split;
+    const int NW = TR / kRPW;
+    const int rpw = kRPW;
+    if (NW < 1 || NW > kMaxWarps || TR % kRPW) return false;
+    const long long tpu = static_cast<long long>(k) * split;
+    const long long T = units * tpu;
+    long long tpc = (T + nsm - 1) / nsm;
+    if (tpc > (kQSlots - 1) * tpu) tpc = (kQSlots - 1) * tpu;  // at most kQSlots units per CTA
+    if (tpc > kMaxTilesPerCta) tpc = kMaxTilesPerCta;
+    if (tpc < 1) tpc = 1;
+    const uint32_t rows_bytes = static_cast<uint32_t>(rpw) * D * es;
+    size_t stage = 2 * static_cast<size_t>(rows_bytes) + (int8 ? 2 * rpw * 4 : 0);
+    const size_t merge_need = static_cast<size_t>(G) * D * 4;
+    if (stage < merge_need) stage = merge_need;
+    stage = align_up(stage, 128);
+    size_t off = align_up(static_cast<size_t>(tpc) * sizeof(TileInfo), 128);
     a->off_q = static_cast<uint32_t>(off);
-    off += S * q_slot;
-    a->off_sc = static_cast<uint32_t>(off);
-    off += S * 2 * sc_tile;
-    a->off_info = static_cast<uint32_t>(off);
-    off += S * 16;
-    a->off_bar = static_cast<uint32_t>(align_up(off, 8));
-    off = a->off_bar + S * 16;
-    a->off_p = static_cast<uint32_t>(align_up(off, 16));
-    off = a->off_p + static_cast<size_t>(kNW) * rpw * G * 8;
-    a->off_alpha = static_cast<uint32_t>(align_up(off, 16));
-    off = a->off_alpha + kNW * G * 4;
-    a->off_merge = static_cast<uint32_t>(align_up(off, 16));
-    off = a->off_merge + (2 * kNW * G + static_cast<size_t>(kNW) * G * D) * 4;
-    pl->smem = off + 1024;
-    a->tile_bytes = tile_bytes;
-    a->q_slot = q_slot;
-    a->sc_tile = sc_tile;
-    a->sc_bytes = int8 ? static_cast<uint32_t>(TR) * N * 4 : 0;
-    const long long T = units * k * pl->split;
-    long long target = nsm < kMaxGrid ? nsm : kMaxGrid;
-    if (target > T) target = T;
-    if (target < 1) target = 1;
-    const long long tpc = (T + target - 1) / target;
+    off = align_up(off + static_cast<size_t>(kQSlots) * G * D * 4, 128);
+    a->off_p = static_cast<uint32_t>(off);
+    off = align_up(off + static_cast<size_t>(NW) * rpw * G * 8, 128);
+    a->off_alpha = static_cast<uint32_t>(off);
+    off = align_up(off + static_cast<size_t>(NW) * G * 4, 16);
+    a->off_ml = static_cast<uint32_t>(off);
+    off = align_up(off + static_cast<size_t>(NW) * 2 * G * 4, 128);
+    a->off_stage = static_cast<uint32_t>(off);
+    long long S = (static_cast<long long>(kSmemBudget) - static_cast<long long>(off)) /
+                  static_cast<long long>(NW * stage);
+    if (S > kMaxStages) S = kMaxStages;
+    if (S < 2) return false;
+    pl->smem = off + static_cast<size_t>(S) * NW * stage;
+    pl->threads = NW * 32;
     pl->grid = static_cast<int>((T + tpc - 1) / tpc);
+    a->stage_bytes = static_cast<uint32_t>(stage);
+    a->rows_bytes = rows_bytes;
     a->T = T;
     a->tpc = static_cast<int>(tpc);
     a->TR = TR;
-    a->split = pl->split;
-    a->S = pl->S;
-    return pl->smem <= static_cast<size_t>(kSmemBudget) + 1024;
+    a->split = split;
+    a->S = static_cast<int>(S);
+    a->NW = NW;
+    a->rpw = rpw;
+    return pl->smem <= static_cast<size_t>(kSmemBudget);
 }
 
 template <Dt KT, int D, int G>
-qs_status launch_attn(const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
-                      const CUtensorMap& ksm, const CUtensorMap& vsm, const AttnPlan& pl,
-                      cudaStream_t s) {
+qs_status launch_attn(const AttnArgs& a, const AttnPlan& pl, cudaStream_t s) {
     auto kern = sparse_attn_kernel<KT, D, G>;
-    if (!ensure_smem(reinterpret_cast<const void*>(kern), pl.smem))
-        return QS_ECUDA;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), pl.smem)) return QS_ECUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.grid);
-    cfg.blockDim = dim3(kThreadsAttn);
+    cfg.blockDim = dim3(pl.threads);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -694,19 +693,17 @@ qs_status launch_attn(const AttnArgs& a, const CUtensorMap& km, const CUtensorMa
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, km, vm, ksm, vsm, a) != cudaSuccess) return QS_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return QS_ECUDA;
     QS_CHECK_LAUNCH();
     return QS_OK;
 }
 
 template <Dt KT, int D>
-qs_status dispatch_g(int G, const AttnArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
-                     const CUtensorMap& ksm, const CUtensorMap& vsm, const AttnPlan& pl,
-                     cudaStream_t s) {
+qs_status dispatch_g(int G, const AttnArgs& a, const AttnPlan& pl, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_attn<KT, D, 1>(a, km, vm, ksm, vsm, pl, s);
-        case 2: return launch_attn<KT, D, 2>(a, km, vm, ksm, vsm, pl, s);
-        case 4: return launch_attn<KT, D, 4>(a, km, vm, ksm, vsm, pl, s);
+        case 1: return launch_attn<KT, D, 1>(a, pl, s);
+        case 2: return launch_attn<KT, D, 2>(a, pl, s);
+        case 4: return launch_attn<KT, D, 4>(a, pl, s);
         default: return QS_EUNSUPPORTED;
     }
 }
@@ -715,10 +712,11 @@ qs_status dispatch_g(int G, const AttnArgs& a, const CUtensorMap& km, const CUte
 
 size_t attn_workspace_bytes(int B, int H, int N, int D, int sel_heads) {
     // counters per unit + one (max, sum, acc) partial slot per (CTA, unit)
-    // pair a stream-K range can produce: at most units + grid slots.
+    // pair of the stream-K split: a slot index is CTA + unit, at most
+    // grid + units - 2, and the planner keeps the grid within units + 1024.
     const long long units = static_cast<long long>(B) * sel_heads;
     const int G = sel_heads == N ? H / N : 1;
-    const long long slots = units + kMaxGrid;
+    const long long slots = 2 * units + 1024;
     return align_up(static_cast<size_t>(units) * 4, 256) +
            align_up(static_cast<size_t>(slots) * G * (D + 2) * 4, 256);
 }
@@ -749,25 +747,31 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
     if (int8 && (!k_scale || !v_scale)) return QS_EINVAL;
     if (D != 64 && D != 128) return QS_EUNSUPPORTED;
     if (D * es < 128) return QS_EUNSUPPORTED;              // a K row spans 8 lanes x 16 B
-    if (BS % 16 || BS > 256 * 8) return QS_EUNSUPPORTED;
-    if (int8 && N % 4) return QS_EUNSUPPORTED;              // scale rows: multiples of 16 B
+    if (BS % 16 || BS > 4096) return QS_EUNSUPPORTED;
+    if (static_cast<long long>(num_kv_blocks) * BS > (1LL << 31) - 1) return QS_EUNSUPPORTED;
     const int G = sel_heads == N ? H / N : 1;
     if (G != 1 && G != 2 && G != 4) return QS_EUNSUPPORTED;
     const int q_es = q_dtype == QS_F32 ? 4 : 2;
     const uintptr_t al = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
-                         reinterpret_cast<uintptr_t>(v_cache) |
-                         (int8 ? reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale) : 0);
+                         reinterpret_cast<uintptr_t>(v_cache);
     if (al % 16) return QS_EINVAL;
+    if (int8 && ((reinterpret_cast<uintptr_t>(k_scale) | reinterpret_cast<uintptr_t>(v_scale)) % 4))
+        return QS_EINVAL;
     const long long units = static_cast<long long>(B) * sel_heads;
     AttnArgs a = {};
     AttnPlan pl = {};
-    if (!plan_attention(BS, D, G, es, q_es, N, int8, units, k, &a, &pl)) return QS_EUNSUPPORTED;
+    if (!plan_attention(BS, D, G, es, q_es, int8, units, k, &a, &pl)) return QS_EUNSUPPORTED;
+    if (pl.grid > units + 1024) return QS_EUNSUPPORTED;   // partial slots: grid + units
     const size_t need = attn_workspace_bytes(B, H, N, D, sel_heads);
     if (!workspace || workspace_bytes < need) return QS_EWORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.q = static_cast<const uint8_t*>(q);
     a.q_dt = q_dtype;
     a.q_es = q_es;
+    a.kc = static_cast<const uint8_t*>(k_cache);
+    a.vc = static_cast<const uint8_t*>(v_cache);
+    a.ks = k_scale;
+    a.vs = v_scale;
     a.bt = block_tables;
     a.MKBPR = MKBPR;
     a.seq_lens = seq_lens;
@@ -782,29 +786,14 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
     a.counters = reinterpret_cast<uint32_t*>(ws);
     a.partial = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(units) * 4, 256));
     a.dev_status = dev_status;
-
-    CUtensorMap km, vm, ksm, vsm;
-    const uint64_t rows = static_cast<uint64_t>(num_kv_blocks) * BS;
-    const uint64_t cols = static_cast<uint64_t>(N) * D;
-    if (!encode_2d(&km, k_cache, es, cols, rows, cols * es, D, a.TR) ||
-        !encode_2d(&vm, v_cache, es, cols, rows, cols * es, D, a.TR))
-        return QS_ECUDA;
-    if (int8) {
-        if (!encode_2d(&ksm, k_scale, 4, N, rows, static_cast<uint64_t>(N) * 4, N, a.TR) ||
-            !encode_2d(&vsm, v_scale, 4, N, rows, static_cast<uint64_t>(N) * 4, N, a.TR))
-            return QS_ECUDA;
-    } else {
-        ksm = km;
-        vsm = vm;
-    }
     switch (kv_dtype) {
-        case QS_F32: return D == 128 ? dispatch_g<Dt::F32, 128>(G, a, km, vm, ksm, vsm, pl, stream)
-                                     : dispatch_g<Dt::F32, 64>(G, a, km, vm, ksm, vsm, pl, stream);
-        case QS_BF16: return D == 128 ? dispatch_g<Dt::BF16, 128>(G, a, km, vm, ksm, vsm, pl, stream)
-                                      : dispatch_g<Dt::BF16, 64>(G, a, km, vm, ksm, vsm, pl, stream);
-        case QS_F16: return D == 128 ? dispatch_g<Dt::F16, 128>(G, a, km, vm, ksm, vsm, pl, stream)
-                                     : dispatch_g<Dt::F16, 64>(G, a, km, vm, ksm, vsm, pl, stream);
-        default: return dispatch_g<Dt::I8, 128>(G, a, km, vm, ksm, vsm, pl, stream);
+        case QS_F32: return D == 128 ? dispatch_g<Dt::F32, 128>(G, a, pl, stream)
+                                     : dispatch_g<Dt::F32, 64>(G, a, pl, stream);
+        case QS_BF16: return D == 128 ? dispatch_g<Dt::BF16, 128>(G, a, pl, stream)
+                                      : dispatch_g<Dt::BF16, 64>(G, a, pl, stream);
+        case QS_F16: return D == 128 ? dispatch_g<Dt::F16, 128>(G, a, pl, stream)
+                                     : dispatch_g<Dt::F16, 64>(G, a, pl, stream);
+        default: return dispatch_g<Dt::I8, 128>(G, a, pl, stream);
     }
 }
 

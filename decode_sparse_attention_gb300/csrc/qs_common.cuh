@@ -104,11 +104,14 @@ QS_DEVINL float ldcg_f32(const float* p) { return __ldcg(p); }
 // ---------------------------------------------------------------------------
 
 QS_DEVINL unsigned long long pack2(float lo, float hi) {
-    return (static_cast<unsigned long long>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
 }
 QS_DEVINL float2 unpack2(unsigned long long v) {
-    return make_float2(__uint_as_float(static_cast<uint32_t>(v)),
-                       __uint_as_float(static_cast<uint32_t>(v >> 32)));
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return make_float2(lo, hi);
 }
 // d = a * b + c, elementwise on two fp32 lanes, each rounded once.
 QS_DEVINL unsigned long long fma2(unsigned long long a, unsigned long long b,
