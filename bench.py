@@ -253,14 +253,22 @@ def setup(w, seed, dev):
     return x, mode, sel, out, params, meta_ms
 
 
-def timed_graph(graph, flush, steps, stream):
+def flush_l2(flush, sink):
+    """Evict the L2: write a buffer twice the L2 size, then read it back, so
+    the next kernel starts with none of its inputs cached and no dirty lines
+    left to write back on its time."""
+    flush.add_(1)
+    torch.sum(flush.view(torch.int32), dim=0, out=sink)
+
+
+def timed_graph(graph, flush, sink, steps, stream):
     """Per-step CUDA-event durations (ms) of graph replays with an L2 flush
     between steps."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     with torch.cuda.stream(stream):     # flush, replay and both events on one stream
         for s, e in evs:
-            flush.zero_()
+            flush_l2(flush, sink)
             s.record(stream)
             graph.replay()
             e.record(stream)
@@ -278,7 +286,8 @@ def run_ours(args, w):
         dist.init_process_group("nccl", device_id=dev)
     qs.lib()
     x, mode, sel, out, params, meta_ms = setup(w, args.seed + rank, dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.zeros((), dtype=torch.int64, device=dev)
     stream = torch.cuda.Stream(dev)
 
     # eager warm-up, then capture the step in a graph
@@ -290,7 +299,24 @@ def run_ours(args, w):
     g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         qs.sparse_decode_step(params, dev)
-    # the dominant kernel alone (same selection, same launch configuration)
+    # the selector alone (diagnostic) and the dominant kernel alone (same
+    # selection, same launch configuration)
+    sel2 = torch.empty_like(sel)
+    g_sel = torch.cuda.CUDAGraph()
+    def run_selector():
+        if mode == 0:
+            qs.quest_block_select_paged_in_out_w(x["q"], x["maxblocks"], x["minblocks"],
+                                                 x["meta_block_tables"], x["seq_lens"], x["t"],
+                                                 sel2)
+        else:
+            qs.probe_select(x["q"], x["k_cache"], x["block_tables"], x["seq_lens"], w.k,
+                            w.n_probe, importance=x.get("importance"),
+                            k_scale=x.get("k_scale"), selected=sel2)
+    with torch.cuda.stream(stream):
+        run_selector()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_sel, stream=stream):
+        run_selector()
     attn_out = torch.empty_like(out)
     g_attn = torch.cuda.CUDAGraph()
     sel_rows = sel.shape[1]
@@ -301,18 +327,19 @@ def run_ours(args, w):
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
-    t_end = time.time() + 1.5
+    t_end = time.time() + args.preroll_s
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2(flush, sink)
             g_step.replay()
         while time.time() < t_end:  # keep the clocks under load for the sampler
             g_step.replay()
     torch.cuda.synchronize()
     barrier()
-    durs = timed_graph(g_step, flush, args.steps, stream)
+    durs = timed_graph(g_step, flush, sink, args.steps, stream)
     barrier()
-    attn_durs = timed_graph(g_attn, flush, max(args.steps // 2, 3), stream)
+    attn_durs = timed_graph(g_attn, flush, sink, max(args.steps // 2, 3), stream)
+    sel_durs = timed_graph(g_sel, flush, sink, max(args.steps // 4, 3), stream)
     clocks = sampler.stop()
     assert qs.read_status(dev) == 0
 
@@ -331,7 +358,7 @@ def run_ours(args, w):
     d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []
     for i in range(max(args.steps // 4, 3) + 3):
-        flush.zero_()
+        flush_l2(flush, sink)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
@@ -365,7 +392,7 @@ def run_ours(args, w):
             "seq_len": w.seq_len if w.seq_len else "ragged", "k": w.k,
             "tokens_since_metadata_update": x["t"], "selector": w.mode,
             "parallelism": "replicas" if ws_ > 1 else "single GPU",
-            "l2": "256 MiB write between timed steps",
+            "l2": "256 MiB written then read back between timed steps",
             "step": "qs_sparse_decode_step replayed as a CUDA graph",
         },
         "step_gbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9, 1),
@@ -385,6 +412,7 @@ def run_ours(args, w):
             "launch_us": round(attn_us, 3),
             "bytes_per_launch": nbytes["attention"],
         },
+        "selector_alone_us": round(1000.0 * statistics.median(sel_durs), 3),
         "metadata_prefill_us": None if meta_ms is None else round(meta_ms * 1000, 2),
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -534,6 +562,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--preroll-s", type=float, default=1.5,
+                    help="seconds of back-to-back steps before the timed loop (clock sampling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -7,26 +7,9 @@
 #include <mutex>
 #include <utility>
 
-#include "qs_common.cuh"
+#include "qs_internal.cuh"
 
 namespace qs {
-
-size_t select_workspace_bytes(int B, int N, int maxnb);
-size_t probe_workspace_bytes(int B, int H, int N, int MKBPR);
-size_t attn_workspace_bytes(int B, int H, int N, int D, int sel_heads);
-qs_status block_select_impl(const void*, qs_dtype, const void*, const void*, qs_dtype,
-                            const int32_t*, int32_t, int32_t, const int32_t*, int32_t, int32_t,
-                            int32_t, int32_t, int32_t, int32_t, int32_t, int32_t*, float*, void*,
-                            size_t, int32_t*, cudaStream_t);
-qs_status probe_select_impl(const void*, qs_dtype, const void*, const float*, qs_dtype, int32_t,
-                            const int32_t*, int32_t, const int32_t*, const float*, int32_t,
-                            int32_t, int32_t, int32_t, int32_t, int32_t, int32_t, int32_t,
-                            int32_t*, void*, size_t, int32_t*, cudaStream_t);
-qs_status sparse_attn_impl(const void*, qs_dtype, const void*, const void*, const float*,
-                           const float*, qs_dtype, int32_t, const int32_t*, int32_t,
-                           const int32_t*, const int32_t*, int32_t, int32_t, float, int32_t,
-                           int32_t, int32_t, int32_t, int32_t, float*, float*, void*, size_t,
-                           int32_t*, cudaStream_t);
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -199,5 +182,5 @@ extern "C" qs_status qs_sparse_decode_step(const qs_step_params* p, qs_stream_t 
                             p->kv_dtype, p->num_kv_blocks, p->block_tables, p->MKBPR, p->seq_lens,
                             p->selected, sel_heads, p->k, p->softmax_scale, p->B, p->H, p->N, p->D,
                             p->BS, p->out, p->lse_opt, ws + sel_ws, p->workspace_bytes - sel_ws,
-                            p->dev_status, s);
+                            p->dev_status, s, /*pdl=*/true);
 }

@@ -26,11 +26,12 @@
 //  * A unit split across CTAs is merged on the device: each CTA writes a
 //    (max, sum, acc) partial; the last to arrive (atomic counter, no spin)
 //    combines them and rearms the counter.
-//  * Launched as a programmatic dependent of the selector: block-table and
-//    query prefetches overlap the selector's tail.
+//  * Inside the fused decode step it is launched as a programmatic dependent
+//    of the selector: ring zeroing, query staging and block-table prefetches
+//    (none of which the selector writes) overlap the selector's tail.
 #include <cmath>
 
-#include "qs_common.cuh"
+#include "qs_internal.cuh"
 
 namespace qs {
 namespace {
@@ -188,6 +189,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
 
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
+    __shared__ int s_split[2];   // units of this CTA shared with other CTAs
+    __shared__ int s_nsplit;
     TileInfo* info = reinterpret_cast<TileInfo*>(smem);
     uint8_t* qslots = smem + a.off_q;
     uint8_t* stages = smem + a.off_stage;
@@ -207,6 +210,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
     const long long u_first = t0 / tpu;
     const int n_units = static_cast<int>((t1 - 1) / tpu - u_first + 1);
     const int G_per_kv = a.H / a.N;
+    if (tid == 0) s_nsplit = 0;
     const size_t qrow_bytes = static_cast<size_t>(G) * D * a.q_es;   // one unit's q rows
     constexpr int kQSlotFloats = G * D;                                  // fp32 copy in smem
 
@@ -223,6 +227,22 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
              o += static_cast<size_t>(nthreads) * 128)
             prefetch_l2(qr + o);
     }
+    {
+        // query rows of the units in range, converted once to fp32
+        float* qf = reinterpret_cast<float*>(qslots);
+        for (int e = tid; e < n_units * kQSlotFloats; e += nthreads) {
+            const int us = e / kQSlotFloats, hd = e % kQSlotFloats;
+            const long long u = u_first + us;
+            const int b = static_cast<int>(u / a.sel_heads), s = static_cast<int>(u % a.sel_heads);
+            const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
+            qf[e] = load_q(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + h0) * D + hd);
+        }
+    }
+    // zero the rings once: rows a warp does not load keep finite contents, so
+    // the unrolled row loops below never read non-finite leftovers
+    for (size_t o = static_cast<size_t>(tid) * 16; o < static_cast<size_t>(a.NW) * S * a.stage_bytes;
+         o += static_cast<size_t>(nthreads) * 16)
+        *reinterpret_cast<uint4*>(stages + o) = make_uint4(0, 0, 0, 0);
     pdl_wait();  // the selection is written by the preceding kernel
 
     // ---- prologue, part 2: tile list and the units' queries
@@ -256,22 +276,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
         }
         info[i] = ti;
     }
-    {
-        // query rows of the units in range, converted once to fp32
-        float* qf = reinterpret_cast<float*>(qslots);
-        for (int e = tid; e < n_units * kQSlotFloats; e += nthreads) {
-            const int us = e / kQSlotFloats, hd = e % kQSlotFloats;
-            const long long u = u_first + us;
-            const int b = static_cast<int>(u / a.sel_heads), s = static_cast<int>(u % a.sel_heads);
-            const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
-            qf[e] = load_q(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + h0) * D + hd);
-        }
-    }
-    // zero the rings once: rows a warp does not load keep finite contents, so
-    // the unrolled row loops below never read non-finite leftovers
-    for (size_t o = static_cast<size_t>(tid) * 16; o < static_cast<size_t>(a.NW) * S * a.stage_bytes;
-         o += static_cast<size_t>(nthreads) * 16)
-        *reinterpret_cast<uint4*>(stages + o) = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
     // ---- per-warp row streams
@@ -563,39 +567,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
                 }
             }
             if (!owned) {
-                __threadfence();
-                __syncthreads();
-                const int c_first = static_cast<int>(ut0 / a.tpc);
-                const int c_last = static_cast<int>((ut1 - 1) / a.tpc);
-                if (tid == 0) {
-                    const uint32_t prev = atomicAdd(&a.counters[u], 1u);
-                    const bool last = prev == static_cast<uint32_t>(c_last - c_first);
-                    if (last) a.counters[u] = 0;
-                    s_last = last;
-                }
-                __syncthreads();
-                if (s_last) {
-                    __threadfence();
-                    for (int idx = tid; idx < G * D; idx += nthreads) {
-                        const int h = idx / D, d = idx % D;
-                        float M = -INFINITY;
-                        for (int cc = c_first; cc <= c_last; ++cc)
-                            M = fmaxf(M, ldcg_f32(a.partial + static_cast<size_t>(cc + u) * G * (D + 2) + h));
-                        float Ls = 0.f, A = 0.f;
-                        if (M != -INFINITY) {
-                            for (int cc = c_first; cc <= c_last; ++cc) {
-                                const float* sl = a.partial + static_cast<size_t>(cc + u) * G * (D + 2);
-                                const float f = exp2_approx(ldcg_f32(sl + h) - M);
-                                Ls += ldcg_f32(sl + G + h) * f;
-                                A += ldcg_f32(sl + 2 * G + h * D + d) * f;
-                            }
-                        }
-                        a.out[(static_cast<size_t>(b) * a.H + h0 + h) * D + d] = Ls > 0.f ? A / Ls : 0.f;
-                        if (d == 0 && a.lse)
-                            a.lse[static_cast<size_t>(b) * a.H + h0 + h] =
-                                Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
-                    }
-                }
+                // shared with other CTAs: merged after the tile loop
+                if (tid == 0) s_split[s_nsplit++] = u;
             }
             // reset the warp state for the next unit
             m_run = -INFINITY;
@@ -608,6 +581,53 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
         }
     }
     cp_async_wait(0);
+
+    // ---- units this CTA shares with others: the last CTA to arrive merges
+    // the (max, sum, acc) partials of all of them
+    __syncthreads();
+    const int nsplit = s_nsplit;
+    if (nsplit > 0) {
+        __threadfence();
+        __syncthreads();
+        for (int k2 = 0; k2 < nsplit; ++k2) {
+            const int u = s_split[k2];
+            const long long ut0 = static_cast<long long>(u) * tpu, ut1 = ut0 + tpu;
+            const int c_first = static_cast<int>(ut0 / a.tpc);
+            const int c_last = static_cast<int>((ut1 - 1) / a.tpc);
+            if (tid == 0) {
+                const uint32_t prev = atomicAdd(&a.counters[u], 1u);
+                const bool last = prev == static_cast<uint32_t>(c_last - c_first);
+                if (last) a.counters[u] = 0;  // rearm for the next call
+                s_last = last;
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                const int b = u / a.sel_heads, s = u % a.sel_heads;
+                const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
+                for (int idx = tid; idx < G * D; idx += nthreads) {
+                    const int h = idx / D, d = idx % D;
+                    float M = -INFINITY;
+                    for (int cc = c_first; cc <= c_last; ++cc)
+                        M = fmaxf(M, ldcg_f32(a.partial + static_cast<size_t>(cc + u) * G * (D + 2) + h));
+                    float Ls = 0.f, A = 0.f;
+                    if (M != -INFINITY) {
+                        for (int cc = c_first; cc <= c_last; ++cc) {
+                            const float* sl = a.partial + static_cast<size_t>(cc + u) * G * (D + 2);
+                            const float f = exp2_approx(ldcg_f32(sl + h) - M);
+                            Ls += ldcg_f32(sl + G + h) * f;
+                            A += ldcg_f32(sl + 2 * G + h * D + d) * f;
+                        }
+                    }
+                    a.out[(static_cast<size_t>(b) * a.H + h0 + h) * D + d] = Ls > 0.f ? A / Ls : 0.f;
+                    if (d == 0 && a.lse)
+                        a.lse[static_cast<size_t>(b) * a.H + h0 + h] =
+                            Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+                }
+            }
+            __syncthreads();
+        }
+    }
 }
 
 struct AttnPlan {
@@ -680,7 +700,7 @@ bool plan_attention(int BS, int D, int G, int es, int q_es, bool int8, long long
 }
 
 template <Dt KT, int D, int G>
-qs_status launch_attn(const AttnArgs& a, const AttnPlan& pl, cudaStream_t s) {
+qs_status launch_attn(const AttnArgs& a, const AttnPlan& pl, bool pdl, cudaStream_t s) {
     auto kern = sparse_attn_kernel<KT, D, G>;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), pl.smem)) return QS_ECUDA;
     cudaLaunchConfig_t cfg = {};
@@ -692,18 +712,18 @@ qs_status launch_attn(const AttnArgs& a, const AttnPlan& pl, cudaStream_t s) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return QS_ECUDA;
     QS_CHECK_LAUNCH();
     return QS_OK;
 }
 
 template <Dt KT, int D>
-qs_status dispatch_g(int G, const AttnArgs& a, const AttnPlan& pl, cudaStream_t s) {
+qs_status dispatch_g(int G, const AttnArgs& a, const AttnPlan& pl, bool pdl, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_attn<KT, D, 1>(a, pl, s);
-        case 2: return launch_attn<KT, D, 2>(a, pl, s);
-        case 4: return launch_attn<KT, D, 4>(a, pl, s);
+        case 1: return launch_attn<KT, D, 1>(a, pl, pdl, s);
+        case 2: return launch_attn<KT, D, 2>(a, pl, pdl, s);
+        case 4: return launch_attn<KT, D, 4>(a, pl, pdl, s);
         default: return QS_EUNSUPPORTED;
     }
 }
@@ -727,7 +747,8 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
                            const int32_t* seq_lens, const int32_t* selected, int32_t sel_heads,
                            int32_t k, float softmax_scale, int32_t B, int32_t H, int32_t N,
                            int32_t D, int32_t BS, float* out, float* lse_opt, void* workspace,
-                           size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+                           size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream,
+                           bool pdl) {
     if (B < 0 || H <= 0 || N <= 0 || H % N != 0 || BS <= 0 || k <= 0 || MKBPR < 0 ||
         num_kv_blocks <= 0)
         return QS_EINVAL;
@@ -787,13 +808,13 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
     a.partial = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(units) * 4, 256));
     a.dev_status = dev_status;
     switch (kv_dtype) {
-        case QS_F32: return D == 128 ? dispatch_g<Dt::F32, 128>(G, a, pl, stream)
-                                     : dispatch_g<Dt::F32, 64>(G, a, pl, stream);
-        case QS_BF16: return D == 128 ? dispatch_g<Dt::BF16, 128>(G, a, pl, stream)
-                                      : dispatch_g<Dt::BF16, 64>(G, a, pl, stream);
-        case QS_F16: return D == 128 ? dispatch_g<Dt::F16, 128>(G, a, pl, stream)
-                                     : dispatch_g<Dt::F16, 64>(G, a, pl, stream);
-        default: return dispatch_g<Dt::I8, 128>(G, a, pl, stream);
+        case QS_F32: return D == 128 ? dispatch_g<Dt::F32, 128>(G, a, pl, pdl, stream)
+                                     : dispatch_g<Dt::F32, 64>(G, a, pl, pdl, stream);
+        case QS_BF16: return D == 128 ? dispatch_g<Dt::BF16, 128>(G, a, pl, pdl, stream)
+                                      : dispatch_g<Dt::BF16, 64>(G, a, pl, pdl, stream);
+        case QS_F16: return D == 128 ? dispatch_g<Dt::F16, 128>(G, a, pl, pdl, stream)
+                                     : dispatch_g<Dt::F16, 64>(G, a, pl, pdl, stream);
+        default: return dispatch_g<Dt::I8, 128>(G, a, pl, pdl, stream);
     }
 }
 
@@ -812,5 +833,6 @@ extern "C" qs_status qs_sparse_decode_attn(const void* q, qs_dtype q_dtype, cons
     return qs::sparse_attn_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, kv_dtype,
                                 num_kv_blocks, block_tables, MKBPR, seq_lens, selected, sel_heads,
                                 k, softmax_scale, B, H, N, D, BS, out, lse_opt, workspace,
-                                workspace_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream));
+                                workspace_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream),
+                                false);
 }

@@ -26,16 +26,9 @@
 // that allocates.
 #include <mutex>
 
-#include "qs_common.cuh"
+#include "qs_internal.cuh"
 
 namespace qs {
-
-qs_status sparse_attn_impl(const void*, qs_dtype, const void*, const void*, const float*,
-                           const float*, qs_dtype, int32_t, const int32_t*, int32_t,
-                           const int32_t*, const int32_t*, int32_t, int32_t, float, int32_t,
-                           int32_t, int32_t, int32_t, int32_t, float*, float*, void*, size_t,
-                           int32_t*, cudaStream_t);
-size_t attn_workspace_bytes(int B, int H, int N, int D, int sel_heads);
 
 namespace {
 
@@ -88,5 +81,5 @@ extern "C" qs_status qs_sparse_decode_attn_noalloc(
     return sparse_attn_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, kv_dtype,
                             num_kv_blocks, block_tables, MKBPR, seq_lens, selected, sel_heads, k,
                             softmax_scale, B, H, N, D, BS, out, lse_opt, scratch,
-                            kStaticScratchBytes, dev_status, s);
+                            kStaticScratchBytes, dev_status, s, false);
 }

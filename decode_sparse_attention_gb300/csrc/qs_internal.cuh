@@ -1,0 +1,40 @@
+// Entry points shared between the translation units of the library.
+#pragma once
+
+#include "qs_common.cuh"
+
+namespace qs {
+
+size_t select_workspace_bytes(int B, int N, int maxnb);
+size_t probe_workspace_bytes(int B, int H, int N, int MKBPR);
+size_t attn_workspace_bytes(int B, int H, int N, int D, int sel_heads);
+
+qs_status block_select_impl(const void* q, qs_dtype q_dtype, const void* maxblocks,
+                            const void* minblocks, qs_dtype meta_dtype,
+                            const int32_t* meta_block_tables, int32_t MMBPR,
+                            int32_t num_meta_blocks, const int32_t* seq_lens, int32_t B,
+                            int32_t H, int32_t N, int32_t D, int32_t BS, int32_t k, int32_t t,
+                            int32_t* selected, float* scores_opt, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+
+qs_status probe_select_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
+                            const float* k_scale, qs_dtype kv_dtype, int32_t num_kv_blocks,
+                            const int32_t* block_tables, int32_t MKBPR, const int32_t* seq_lens,
+                            const float* importance, int32_t importance_stride, int32_t B,
+                            int32_t H, int32_t N, int32_t D, int32_t BS, int32_t k,
+                            int32_t n_probe, int32_t* selected, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
+
+// pdl: launch as a programmatic dependent of the kernel before it on the
+// stream (only when that kernel writes nothing the attention reads before
+// its grid-dependency wait, i.e. after the selectors).
+qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
+                           const void* v_cache, const float* k_scale, const float* v_scale,
+                           qs_dtype kv_dtype, int32_t num_kv_blocks, const int32_t* block_tables,
+                           int32_t MKBPR, const int32_t* seq_lens, const int32_t* selected,
+                           int32_t sel_heads, int32_t k, float softmax_scale, int32_t B, int32_t H,
+                           int32_t N, int32_t D, int32_t BS, float* out, float* lse_opt,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           cudaStream_t stream, bool pdl);
+
+}  // namespace qs

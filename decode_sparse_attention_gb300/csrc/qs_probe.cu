@@ -12,17 +12,22 @@
 //
 // GB300 design: grid = (block chunks, B*N).  A CTA scores a chunk of blocks
 // for all H/N query heads of one KV head, so each probed K row is read once
-// for the whole group.  The last CTA of a (request, KV head) runs the
-// selection for its query heads: two CTA-wide radix top-k passes (importance,
-// then probe) and a min-reduction for the recency eviction.
-#include "qs_common.cuh"
+// for the whole group; every lane group has all probe rows of its two blocks
+// in flight at once.  A unit of 2..8 chunks runs as a thread-block cluster
+// whose CTAs write their probe scores into the leader CTA's shared memory
+// (larger units use a global buffer and an arrival counter).  The leader
+// then selects for each query head: histogram top-k passes for the
+// importance picks and the probe fill, a min-reduction for the recency
+// eviction, and one warp writes the indices in ascending order.
+#include <cooperative_groups.h>
+
+#include "qs_internal.cuh"
 #include "qs_topk.cuh"
 
 namespace qs {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBlocksPerChunk = 8;
 constexpr int kMaxG = 8;
 
 struct ProbeArgs {
@@ -76,19 +81,32 @@ template <Dt T, int G> struct ProbeChunk16 {
 template <int G> struct ProbeChunk<Dt::BF16, G> : ProbeChunk16<Dt::BF16, G> {};
 template <int G> struct ProbeChunk<Dt::F16, G> : ProbeChunk16<Dt::F16, G> {};
 
-template <Dt KT, int D, int G>
+enum Mode : int { kSingle = 0, kCluster = 1, kGlobal = 2 };
+
+// Blocks one CTA scores: every lane group (one K row per group) takes two
+// blocks and has all their probe rows in flight at once.
+template <Dt KT, int D> constexpr int blocks_per_chunk() {
+    return 2 * (kThreads / (D * DtInfo<KT>::bytes / 16));
+}
+constexpr int kProbeBatch = 8;     // probe rows of one block loaded together
+
+template <Dt KT, int D, int G, int MODE>
 __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     constexpr bool kInt8 = KT == Dt::I8;
     constexpr int kElemBytes = DtInfo<KT>::bytes;
     constexpr int kLanesPerRow = D * kElemBytes / 16;
     constexpr int kEl = 16 / kElemBytes;  // elements per 16-byte chunk
     constexpr int kGroups = kThreads / kLanesPerRow;
+    constexpr int kBlocksPerChunk = blocks_per_chunk<KT, D>();
     static_assert(kLanesPerRow >= 1 && kLanesPerRow <= 32, "row must span 1..32 lanes");
 
+    // dynamic: probe keys [G][MKBPR] u32, importance keys [MKBPR] u32,
+    // flags [MKBPR] u8, importance flags [MKBPR] u8
     extern __shared__ __align__(16) uint8_t dyn[];
     __shared__ __align__(16) float s_q[G][D];
     __shared__ __align__(16) int8_t s_q8[G][D];
     __shared__ float s_sq[G];
+    __shared__ TopkFastScratch s_fast;
     __shared__ TopkScratch<kThreads> s_topk;
     __shared__ int s_last;
 
@@ -100,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     const int L = a.seq_lens[b];
     const bool bad_len = L < 0 || L > a.MKBPR * BS ||
                          (a.importance != nullptr && L > a.imp_stride);
-    if (bad_len) {
+    if (bad_len) {   // uniform over the unit's CTAs
         if (blockIdx.x == 0) {
             if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_ESEQ_LEN);
             for (int i = threadIdx.x; i < G * a.k; i += kThreads)
@@ -110,8 +128,16 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     }
     const int nb = (L + BS - 1) / BS;
     const int n_chunks = max(1, (nb + kBlocksPerChunk - 1) / kBlocksPerChunk);
-    if (static_cast<int>(blockIdx.x) >= n_chunks) return;
+    if (MODE != kCluster && static_cast<int>(blockIdx.x) >= n_chunks) return;
     const int n_probe = max(1, a.n_probe);
+    uint32_t* pkeys = reinterpret_cast<uint32_t*>(dyn);
+    uint32_t* ikeys = pkeys + static_cast<size_t>(G) * a.MKBPR;
+    uint8_t* flags = reinterpret_cast<uint8_t*>(ikeys + a.MKBPR);
+    uint8_t* imp_flags = flags + a.MKBPR;
+    uint32_t* dst_pkeys = pkeys;
+    if constexpr (MODE == kCluster)
+        dst_pkeys = cooperative_groups::this_cluster().map_shared_rank(pkeys, 0);
+    topk_fast_clear<kThreads>(s_fast);
 
     // queries of the group (fp32), plus the int8 quantisation for int8 caches
     for (int i = threadIdx.x; i < G * D; i += kThreads) {
@@ -119,8 +145,8 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         s_q[h][d] = load_q(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + n * G + h) * D + d);
     }
     __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if constexpr (kInt8) {
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         for (int h = warp; h < G; h += kThreads / 32) {
             float amax = 0.f;
             for (int d = lane; d < D; d += 32) amax = fmaxf(amax, fabsf(s_q[h][d]));
@@ -137,8 +163,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         __syncthreads();
     }
 
-    // probe scores of this chunk's blocks
-    const int lane = threadIdx.x & 31;
+    // ---- probe scores of this chunk's blocks (two blocks per lane group)
     const int grp = threadIdx.x / kLanesPerRow;
     const int cl = threadIdx.x % kLanesPerRow;
     const unsigned gmask = kLanesPerRow == 32
@@ -158,65 +183,107 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         }
     }
     const size_t row_bytes = static_cast<size_t>(a.N) * D * kElemBytes;
-    const int j_begin = blockIdx.x * kBlocksPerChunk;
-    const int j_end = min(nb, j_begin + kBlocksPerChunk);
-    for (int j = j_begin + grp; j < j_end; j += kGroups) {
-        const int p = a.bt[static_cast<size_t>(b) * a.MKBPR + j];
+    const int j_base = blockIdx.x * kBlocksPerChunk + grp;
+    int p_blk[2], p0s[2], steps[2], nps[2];
+    uint4 v[2][kProbeBatch];
+    float sk[2][kProbeBatch];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int j = j_base + jj * kGroups;
+        nps[jj] = 0;
+        p_blk[jj] = -1;
+        if (j < nb) {
+            const int p = a.bt[static_cast<size_t>(b) * a.MKBPR + j];
+            if (p < 0 || p >= a.num_kv_blocks) {
+                if (cl == 0) set_status(a.dev_status, QS_DEV_EBLOCK_TABLE);
+            } else {
+                const int p0 = j * BS, p_end = min(p0 + BS, L);
+                steps[jj] = max(1, (p_end - p0) / n_probe);
+                nps[jj] = (p_end - p0 + steps[jj] - 1) / steps[jj];
+                p_blk[jj] = p;
+                p0s[jj] = p0;
+            }
+        }
+    }
+    // first batch of both blocks in flight together
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const uint8_t* base = a.k_cache + static_cast<size_t>(max(p_blk[jj], 0)) * BS * row_bytes +
+                              static_cast<size_t>(n) * D * kElemBytes + cl * 16;
+#pragma unroll
+        for (int i = 0; i < kProbeBatch; ++i) {
+            v[jj][i] = make_uint4(0, 0, 0, 0);
+            sk[jj][i] = 0.f;
+            if (i < nps[jj]) {
+                const int t = i * steps[jj];
+                v[jj][i] = ldg_stream(base + static_cast<size_t>(t) * row_bytes);
+                if constexpr (kInt8) sk[jj][i] = a.k_scale[(static_cast<size_t>(p_blk[jj]) * BS + t) * a.N + n];
+            }
+        }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int j = j_base + jj * kGroups;
         float best[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) best[h] = -1e30f;
-        if (p < 0 || p >= a.num_kv_blocks) {
-            if (cl == 0) set_status(a.dev_status, QS_DEV_EBLOCK_TABLE);
-        } else {
-            const int p0 = j * BS;
-            const int p_end = min(p0 + BS, L);
-            const int step = max(1, (p_end - p0) / n_probe);
-            const uint8_t* base = a.k_cache + static_cast<size_t>(p) * BS * row_bytes +
-                                  static_cast<size_t>(n) * D * kElemBytes + cl * 16;
-            for (int ps = p0; ps < p_end; ps += step) {
-                const int t = ps - p0;
-                const uint4 v = ldg_stream(base + static_cast<size_t>(t) * row_bytes);
-                if constexpr (kInt8) {
-                    int acc[G];
-                    const int w[4] = {static_cast<int>(v.x), static_cast<int>(v.y),
-                                      static_cast<int>(v.z), static_cast<int>(v.w)};
+        for (int i0 = 0; i0 < nps[jj]; i0 += kProbeBatch) {
+            if (i0 > 0) {   // more probes than one batch (short final block)
+                const uint8_t* base = a.k_cache + static_cast<size_t>(p_blk[jj]) * BS * row_bytes +
+                                      static_cast<size_t>(n) * D * kElemBytes + cl * 16;
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        acc[h] = 0;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[h] = __dp4a(q8r[h][i], w[i], acc[h]);
-#pragma unroll
-                        for (int o = kLanesPerRow / 2; o >= 1; o >>= 1)
-                            acc[h] += __shfl_xor_sync(gmask, acc[h], o);
+                for (int i = 0; i < kProbeBatch; ++i)
+                    if (i0 + i < nps[jj]) {
+                        const int t = (i0 + i) * steps[jj];
+                        v[jj][i] = ldg_stream(base + static_cast<size_t>(t) * row_bytes);
+                        if constexpr (kInt8)
+                            sk[jj][i] = a.k_scale[(static_cast<size_t>(p_blk[jj]) * BS + t) * a.N + n];
                     }
-                    const float sk = a.k_scale[(static_cast<size_t>(p) * BS + t) * a.N + n];
+            }
+#pragma unroll
+            for (int i = 0; i < kProbeBatch; ++i) {
+                if (i0 + i >= nps[jj]) break;
+                if constexpr (kInt8) {
+                    const int w[4] = {static_cast<int>(v[jj][i].x), static_cast<int>(v[jj][i].y),
+                                      static_cast<int>(v[jj][i].z), static_cast<int>(v[jj][i].w)};
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
-                        const float dot = __fmul_rn(__fmul_rn(s_sq[h], sk), static_cast<float>(acc[h]));
+                        int acc = 0;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc = __dp4a(q8r[h][e], w[e], acc);
+#pragma unroll
+                        for (int o = kLanesPerRow / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(gmask, acc, o);
+                        const float dot = __fmul_rn(__fmul_rn(s_sq[h], sk[jj][i]), static_cast<float>(acc));
                         best[h] = fmaxf(best[h], dot);
                     }
                 } else {
                     float acc[G];
 #pragma unroll
                     for (int h = 0; h < G; ++h) acc[h] = 0.f;
-                    ProbeChunk<KT, G>::dot(qr, v, acc);
+                    ProbeChunk<KT, G>::dot(qr, v[jj][i], acc);
 #pragma unroll
                     for (int h = 0; h < G; ++h) {
 #pragma unroll
-                        for (int o = kLanesPerRow / 2; o >= 1; o >>= 1)
-                            acc[h] += __shfl_xor_sync(gmask, acc[h], o);
+                        for (int o = kLanesPerRow / 2; o >= 1; o >>= 1) acc[h] += __shfl_xor_sync(gmask, acc[h], o);
                         best[h] = fmaxf(best[h], acc[h]);
                     }
                 }
             }
         }
-        if (cl == 0)
+        if (cl == 0 && j < nb) {
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-                a.probe[(static_cast<size_t>(b) * a.H + n * G + h) * a.MKBPR + j] = best[h];
+            for (int h = 0; h < G; ++h) {
+                if (MODE != kGlobal) dst_pkeys[h * a.MKBPR + j] = float_key(best[h]);
+                else a.probe[(static_cast<size_t>(b) * a.H + n * G + h) * a.MKBPR + j] = best[h];
+            }
+        }
     }
 
-    if (n_chunks > 1) {
+    // ---- all probe scores of the unit in the leader's shared memory
+    if constexpr (MODE == kCluster) {
+        cooperative_groups::this_cluster().sync();
+        if (blockIdx.x != 0) return;
+    } else if constexpr (MODE == kGlobal) {
         __threadfence();
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -227,51 +294,50 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         __syncthreads();
         if (!s_last) return;
         __threadfence();
+        for (int e = threadIdx.x; e < G * nb; e += kThreads) {
+            const int h = e / nb, j = e % nb;
+            pkeys[h * a.MKBPR + j] =
+                float_key(ldcg_f32(a.probe + (static_cast<size_t>(b) * a.H + n * G + h) * a.MKBPR + j));
+        }
     } else {
         __syncthreads();
     }
 
-    // selection for the G query heads of this KV head
-    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
-    uint8_t* imp_flags = dyn + static_cast<size_t>(a.MKBPR) * 4;
-    uint8_t* flags = imp_flags + a.MKBPR;
-    int n_imp = 0;
-    if (a.importance) {
-        // summed prefill importance per block, fp32 in token order
-        for (int j = threadIdx.x; j < nb; j += kThreads) {
+    // ---- importance pre-selection (same for every head of the request)
+    const int n_imp = a.importance ? min((a.k + 1) / 2, nb) : 0;
+    for (int j = threadIdx.x; j < nb; j += kThreads) {
+        imp_flags[j] = kCand;
+        if (a.importance) {
+            // summed prefill importance of the block, fp32 in token order
             const int p0 = j * BS, p_end = min(p0 + BS, L);
-            float s = 0.f;
             const float* imp = a.importance + static_cast<size_t>(b) * a.imp_stride;
-            for (int ps = p0; ps < p_end; ++ps) s = __fadd_rn(s, imp[ps]);
-            keys[j] = float_key(s);
-            imp_flags[j] = kCand;
+            float sacc = 0.f;
+            for (int ps = p0; ps < p_end; ++ps) sacc = __fadd_rn(sacc, imp[ps]);
+            ikeys[j] = float_key(sacc);
         }
-        __syncthreads();
-        n_imp = min((a.k + 1) / 2, nb);
-        topk_flags<kThreads>(keys, imp_flags, nb, n_imp, s_topk);
-        for (int j = threadIdx.x; j < nb; j += kThreads)
-            imp_flags[j] = (imp_flags[j] & kPick) ? kFixed : 0;
-    } else {
-        for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = 0;
     }
     __syncthreads();
+    if (n_imp > 0) topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
+    for (int j = threadIdx.x; j < nb; j += kThreads)
+        imp_flags[j] = (imp_flags[j] & kPick) ? kFixed : 0;
+    const int want = min(a.k - n_imp, nb - n_imp);
+
+    // ---- per query head: probe fill, recency insurance, ordered output
     for (int h = 0; h < G; ++h) {
         const size_t row = static_cast<size_t>(b) * a.H + n * G + h;
-        for (int j = threadIdx.x; j < nb; j += kThreads) {
-            keys[j] = float_key(ldcg_f32(a.probe + row * a.MKBPR + j));
-            flags[j] = imp_flags[j] ? kFixed : kCand;
-        }
+        const uint32_t* keys = pkeys + static_cast<size_t>(h) * a.MKBPR;
+        topk_fast_clear<kThreads>(s_fast);
+        for (int j = threadIdx.x; j < nb; j += kThreads) flags[j] = imp_flags[j] ? kFixed : kCand;
         __syncthreads();
-        const int want = min(a.k - n_imp, nb - n_imp);
-        topk_flags<kThreads>(keys, flags, nb, want, s_topk);
-        // recency insurance
+        topk_fast<kThreads>(keys, flags, nb, want, s_fast, s_topk);
         if (want > 0 && !(flags[nb - 1] & (kFixed | kPick))) {
+            // the last block replaces the probe pick with the lowest probe
+            // score (ties: the larger index); importance picks stay
             if (threadIdx.x == 0) s_topk.best = ~0ull;
             __syncthreads();
             unsigned long long mine = ~0ull;
             for (int j = threadIdx.x; j < nb; j += kThreads)
                 if (flags[j] & kPick) {
-                    // smallest probe score first, then the larger index
                     const unsigned long long c =
                         (static_cast<unsigned long long>(keys[j]) << 32) | (0xffffffffu - static_cast<uint32_t>(j));
                     mine = c < mine ? c : mine;
@@ -285,22 +351,41 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
             }
             __syncthreads();
         }
-        emit_sorted<kThreads>(flags, kFixed | kPick, nb, a.k, a.selected + row * a.k, s_topk);
+        if (warp == 0) warp_emit_flags(flags, kFixed | kPick, nb, a.k, a.selected + row * a.k);
+        __syncthreads();
     }
+}
+
+template <Dt KT, int D, int G, int MODE>
+qs_status launch_mode(const ProbeArgs& a, int chunks, size_t smem, cudaStream_t s) {
+    auto kern = probe_select_kernel<KT, D, G, MODE>;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return QS_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(chunks, a.B * a.N);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = chunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = MODE == kCluster ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return QS_ECUDA;
+    QS_CHECK_LAUNCH();
+    return QS_OK;
 }
 
 template <Dt KT, int D, int G>
 qs_status launch(const ProbeArgs& a, cudaStream_t s) {
-    const size_t smem = align_up(static_cast<size_t>(a.MKBPR) * 6, 16);
+    const size_t smem = align_up(static_cast<size_t>(a.MKBPR) * (4 * G + 4 + 2), 16);
     if (smem > 160 * 1024) return QS_EUNSUPPORTED;
-    auto kern = probe_select_kernel<KT, D, G>;
-    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem))
-        return QS_ECUDA;
+    constexpr int kBlocksPerChunk = blocks_per_chunk<KT, D>();
     const int chunks = max(1, (a.MKBPR + kBlocksPerChunk - 1) / kBlocksPerChunk);
-    dim3 grid(chunks, a.B * a.N);
-    kern<<<grid, kThreads, smem, s>>>(a);
-    QS_CHECK_LAUNCH();
-    return QS_OK;
+    if (chunks == 1) return launch_mode<KT, D, G, kSingle>(a, chunks, smem, s);
+    if (chunks <= 8) return launch_mode<KT, D, G, kCluster>(a, chunks, smem, s);
+    return launch_mode<KT, D, G, kGlobal>(a, chunks, smem, s);
 }
 
 template <Dt KT, int D>

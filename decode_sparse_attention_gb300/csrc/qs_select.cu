@@ -7,23 +7,33 @@
 // plus the '_in_out_w' sink + window forcing driven by
 // tokens_since_metadata_update.
 //
-// GB300 design: the scan of the metadata rows is the whole cost, so it is
-// spread over many CTAs: grid = (row chunks, B*N units).  Each CTA scores one
-// chunk of rows of one (request, KV head) with 128-bit streaming loads (a row
-// of one head is D*elem bytes, read by D*elem/16 lanes; several rows in flight
-// per lane) and writes fp32 scores to a buffer.  The last CTA of a unit to
-// finish (atomic arrival counter, no spinning) runs the CTA-wide radix top-k
-// and writes the selection.  The counter is reset by that CTA, so the
-// workspace stays zeroed between calls.
-#include "qs_common.cuh"
+// GB300 design: the scan of the metadata rows is the whole cost, so each
+// (request, KV head) is split into row chunks of one load step each: every
+// lane keeps 8 rows of max/min in flight with 128-bit streaming loads and
+// computes the group-mean query of its own 16-byte slice of D.  A unit of
+// one chunk scores into shared memory; a unit of 2..8 chunks runs as one
+// thread-block cluster whose CTAs write their scores straight into the
+// leader CTA's shared memory (distributed shared memory) before a cluster
+// barrier; larger units fall back to a global score buffer and an arrival
+// counter.  The leader then selects with a histogram top-k (one 1024-bin
+// pass, exact ranking inside the boundary bin) and one warp writes the
+// indices in ascending order.
+#include <cooperative_groups.h>
+
+#include "qs_internal.cuh"
 #include "qs_topk.cuh"
 
 namespace qs {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRowsPerChunk = 64;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;     // rows in flight per lane: a chunk loads in one step
+constexpr int kMaxG = 8;       // query heads per KV head
+
+// Rows of one chunk: every lane group keeps kUnroll rows in flight.
+template <Dt MT, int D> constexpr int rows_per_chunk() {
+    return (kThreads / 32) * (32 / (D * DtInfo<MT>::bytes / 16)) * kUnroll;
+}
 
 struct SelectArgs {
     const void* q;
@@ -36,6 +46,7 @@ struct SelectArgs {
     int B, H, N, BS, k, t;
     int32_t* selected;
     float* scores;        // [B*N, maxnb]
+    bool scores_out;      // the caller asked for the scores
     uint32_t* counters;   // [B*N]
     int32_t* dev_status;
 };
@@ -83,16 +94,48 @@ template <Dt T> struct RowChunk16 {
 template <> struct RowChunk<Dt::BF16> : RowChunk16<Dt::BF16> {};
 template <> struct RowChunk<Dt::F16> : RowChunk16<Dt::F16> {};
 
-template <Dt MT, int D>
-__global__ void __launch_bounds__(kThreads) quest_select_kernel(SelectArgs a) {
+// kEl query elements of one head starting at element `off`, as fp32.
+template <int kEl>
+QS_DEVINL void load_q_slice(const void* q, int q_dt, size_t off, float (&out)[kEl]) {
+    if (q_dt == QS_F32) {
+        const float* p = static_cast<const float*>(q) + off;
+#pragma unroll
+        for (int e = 0; e < kEl; e += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(p + e);
+            out[e] = v.x; out[e + 1] = v.y; out[e + 2] = v.z; out[e + 3] = v.w;
+        }
+    } else {
+        const uint16_t* p = static_cast<const uint16_t*>(q) + off;
+        uint32_t w[kEl / 2];
+        if constexpr (kEl == 8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(p);
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(p);
+            w[0] = v.x; w[1] = v.y;
+        }
+#pragma unroll
+        for (int i = 0; i < kEl / 2; ++i) {
+            const float2 f = q_dt == QS_BF16 ? pair_to_float2<Dt::BF16>(w[i]) : pair_to_float2<Dt::F16>(w[i]);
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+}
+
+enum Mode : int { kSingle = 0, kCluster = 1, kGlobal = 2 };
+
+template <Dt MT, int D, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) quest_select_kernel(SelectArgs a) {
     constexpr int kElemBytes = DtInfo<MT>::bytes;
     constexpr int kLanesPerRow = D * kElemBytes / 16;   // 8, 16 or 32
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
     constexpr int kEl = RowChunk<MT>::kElems;
+    constexpr int kRowsPerChunk = rows_per_chunk<MT, D>();
     static_assert(kLanesPerRow >= 1 && kLanesPerRow <= 32, "row must span 1..32 lanes");
 
-    extern __shared__ __align__(16) uint8_t dyn[];
-    __shared__ float s_qg[D];
+    extern __shared__ __align__(16) uint8_t dyn[];   // keys [maxnb] u32, flags [maxnb] u8
+    __shared__ TopkFastScratch s_fast;
     __shared__ TopkScratch<kThreads> s_topk;
     __shared__ int s_last;
 
@@ -104,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) quest_select_kernel(SelectArgs a) {
     const int maxnb = a.MMBPR * BS;
     const int L = a.seq_lens[b];
     int32_t* sel_out = a.selected + static_cast<size_t>(u) * a.k;
-    if (L < 0 || (L + BS - 1) / BS > maxnb) {
+    if (L < 0 || (L + BS - 1) / BS > maxnb) {   // uniform over the unit's CTAs
         if (blockIdx.x == 0) {
             if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_ESEQ_LEN);
             for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;
@@ -113,63 +156,116 @@ __global__ void __launch_bounds__(kThreads) quest_select_kernel(SelectArgs a) {
     }
     const int nb = (L + BS - 1) / BS;
     const int n_chunks = max(1, (nb + kRowsPerChunk - 1) / kRowsPerChunk);
-    if (static_cast<int>(blockIdx.x) >= n_chunks) return;
+    if (MODE != kCluster && static_cast<int>(blockIdx.x) >= n_chunks) return;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
+    uint8_t* flags = dyn + static_cast<size_t>(maxnb) * 4;
+    topk_fast_clear<kThreads>(s_fast);
 
-    // step 1: group-mean query of KV head n
-    const int G = a.H / a.N;
-    for (int d = threadIdx.x; d < D; d += kThreads) {
-        float s = 0.f;
-        for (int g = 0; g < G; ++g)
-            s += load_q(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + n * G + g) * D + d);
-        s_qg[d] = s / static_cast<float>(G);
-    }
-    __syncthreads();
-
-    // steps 2.1-2.2: score this chunk's rows
+    // steps 1, 2.1, 2.2
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane / kLanesPerRow;          // row slot within the warp
     const int cl = lane % kLanesPerRow;           // 16-byte chunk within the row
-    float qreg[kEl];
-#pragma unroll
-    for (int i = 0; i < kEl; ++i) qreg[i] = s_qg[cl * kEl + i];
+    const int G = a.H / a.N;
     const size_t head_off = static_cast<size_t>(n) * D * kElemBytes + static_cast<size_t>(cl) * 16;
     const size_t row_stride = static_cast<size_t>(a.N) * D * kElemBytes;
     const int j_begin = blockIdx.x * kRowsPerChunk;
     const int j_end = min(nb, j_begin + kRowsPerChunk);
-    constexpr int kRowsPerStep = (kThreads / 32) * kRowsPerWarp * kUnroll;
     float* scores_u = a.scores + static_cast<size_t>(u) * maxnb;
-    for (int j0 = j_begin; j0 < j_end; j0 += kRowsPerStep) {
-        uint4 vmx[kUnroll], vmn[kUnroll];
-        bool live[kUnroll];
+    uint32_t* dst_keys = keys;
+    if constexpr (MODE == kCluster)
+        dst_keys = cooperative_groups::this_cluster().map_shared_rank(keys, 0);
+    // Table entries and the G heads' query slices are all requested before
+    // either is used (in-order issue would otherwise serialise the round
+    // trips); the metadata rows follow once the table entries are back.
+    int mrow[kUnroll];
 #pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const int j = j0 + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
-            live[r] = j < j_end;
-            vmx[r] = vmn[r] = make_uint4(0, 0, 0, 0);
-            if (live[r]) {
-                const int m = a.mbt[static_cast<size_t>(b) * a.MMBPR + j / BS];
-                if (m < 0 || m >= a.num_meta) {
-                    set_status(a.dev_status, QS_DEV_EMETA_TABLE);
-                    live[r] = false;
-                } else {
-                    const size_t off = (static_cast<size_t>(m) * BS + j % BS) * row_stride + head_off;
-                    vmx[r] = ldg_stream(a.maxb + off);
-                    vmn[r] = ldg_stream(a.minb + off);
+    for (int r = 0; r < kUnroll; ++r) {
+        const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
+        mrow[r] = j < j_end ? a.mbt[static_cast<size_t>(b) * a.MMBPR + j / BS] : -1;
+    }
+    constexpr int kQBytes = kEl * 4;                 // fp32 query slice; 16-bit uses half
+    constexpr int kQVec = (kQBytes + 15) / 16;       // 16-byte loads per head slice
+    uint4 qraw[kMaxG][kQVec];
+    const int q_es = a.q_dt == QS_F32 ? 4 : 2;
+    const uint8_t* qbase = static_cast<const uint8_t*>(a.q) +
+                           ((static_cast<size_t>(b) * a.H + static_cast<size_t>(n) * G) * D + cl * kEl) * q_es;
+#pragma unroll
+    for (int g = 0; g < kMaxG; ++g)
+#pragma unroll
+        for (int v = 0; v < kQVec; ++v) {
+            qraw[g][v] = make_uint4(0, 0, 0, 0);
+            if (g < G && v * 16 < kEl * q_es) {
+                const uint8_t* p = qbase + static_cast<size_t>(g) * D * q_es + v * 16;
+                if (kEl * q_es >= 16) qraw[g][v] = *reinterpret_cast<const uint4*>(p);
+                else {
+                    const uint2 h = *reinterpret_cast<const uint2*>(p);
+                    qraw[g][v] = make_uint4(h.x, h.y, 0, 0);
+                }
+            }
+        }
+    // group-mean query of this lane's slice
+    float qreg[kEl];
+    {
+        float acc[kEl];
+#pragma unroll
+        for (int e = 0; e < kEl; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int g = 0; g < kMaxG; ++g) {
+            if (g >= G) break;
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(&qraw[g][0]);
+            if (a.q_dt == QS_F32) {
+#pragma unroll
+                for (int e = 0; e < kEl; ++e) acc[e] += __uint_as_float(w[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kEl / 2; ++e) {
+                    const float2 f = a.q_dt == QS_BF16 ? pair_to_float2<Dt::BF16>(w[e])
+                                                       : pair_to_float2<Dt::F16>(w[e]);
+                    acc[2 * e] += f.x;
+                    acc[2 * e + 1] += f.y;
                 }
             }
         }
 #pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const int j = j0 + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
-            float s = RowChunk<MT>::dot(qreg, vmx[r], vmn[r]);
+        for (int e = 0; e < kEl; ++e) qreg[e] = acc[e] / static_cast<float>(G);
+    }
+    uint4 vmx[kUnroll], vmn[kUnroll];
+    bool live[kUnroll];
 #pragma unroll
-            for (int o = kLanesPerRow / 2; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (cl == 0 && j < j_end) scores_u[j] = live[r] ? s : __int_as_float(0xff800000);
+    for (int r = 0; r < kUnroll; ++r) {
+        const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
+        const int m = mrow[r];
+        live[r] = j < j_end;
+        vmx[r] = vmn[r] = make_uint4(0, 0, 0, 0);
+        if (live[r]) {
+            if (m < 0 || m >= a.num_meta) {
+                set_status(a.dev_status, QS_DEV_EMETA_TABLE);
+                live[r] = false;
+            } else {
+                const size_t off = (static_cast<size_t>(m) * BS + j % BS) * row_stride + head_off;
+                vmx[r] = ldg_stream(a.maxb + off);
+                vmn[r] = ldg_stream(a.minb + off);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r) {
+        const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
+        float s = RowChunk<MT>::dot(qreg, vmx[r], vmn[r]);
+#pragma unroll
+        for (int o = kLanesPerRow / 2; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (cl == 0 && j < j_end) {
+            const float v = live[r] ? s : __int_as_float(0xff800000);
+            if (MODE != kGlobal) dst_keys[j] = float_key(v);
+            if (MODE == kGlobal || a.scores_out) scores_u[j] = v;
         }
     }
 
-    // arrival: the last chunk of the unit selects
-    if (n_chunks > 1) {
+    // all scores of the unit in the leader's shared memory
+    if constexpr (MODE == kCluster) {
+        cooperative_groups::this_cluster().sync();
+        if (blockIdx.x != 0) return;
+    } else if constexpr (MODE == kGlobal) {
         __threadfence();
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -180,48 +276,60 @@ __global__ void __launch_bounds__(kThreads) quest_select_kernel(SelectArgs a) {
         __syncthreads();
         if (!s_last) return;
         __threadfence();
-    } else {
-        __syncthreads();
+        for (int j = threadIdx.x; j < nb; j += kThreads) keys[j] = float_key(ldcg_f32(scores_u + j));
     }
 
-    // step 2.3 + window: keys and flags in shared memory
-    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
-    uint8_t* flags = dyn + static_cast<size_t>(maxnb) * 4;
+    // step 2.3 + window
     int w0 = nb;  // first window block (nb: none)
     if (a.t >= 0 && nb > 0) {
         w0 = L - a.t >= 0 ? (L - a.t) / BS : 0;
         w0 = min(w0, nb - 1);
     }
-    for (int j = threadIdx.x; j < nb; j += kThreads) {
-        keys[j] = float_key(ldcg_f32(scores_u + j));
-        const bool forced = a.t >= 0 && (j == 0 || j >= w0);
-        flags[j] = forced ? kFixed : kCand;
-    }
-    __syncthreads();
     const int n_forced = a.t >= 0 && nb > 0 ? (nb - w0) + (w0 > 0 ? 1 : 0) : 0;
     if (n_forced > a.k) {
         if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_EFORCED);
         for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;
         return;
     }
+    for (int j = threadIdx.x; j < nb; j += kThreads)
+        flags[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
+    __syncthreads();
     const int want = min(a.k - n_forced, nb - n_forced);
-    topk_flags<kThreads>(keys, flags, nb, want, s_topk);
-    emit_sorted<kThreads>(flags, kFixed | kPick, nb, a.k, sel_out, s_topk);
+    topk_fast<kThreads>(keys, flags, nb, want, s_fast, s_topk);
+    if (warp == 0) warp_emit_flags(flags, kFixed | kPick, nb, a.k, sel_out);
+}
+
+template <Dt MT, int D, int MODE>
+qs_status launch_mode(const SelectArgs& a, int chunks, size_t smem, cudaStream_t s) {
+    auto kern = quest_select_kernel<MT, D, MODE>;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return QS_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(chunks, a.B * a.N);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = chunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = MODE == kCluster ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return QS_ECUDA;
+    QS_CHECK_LAUNCH();
+    return QS_OK;
 }
 
 template <Dt MT, int D>
 qs_status launch(const SelectArgs& a, cudaStream_t s) {
     const int maxnb = a.MMBPR * a.BS;
     const size_t smem = align_up(static_cast<size_t>(maxnb) * 5, 16);
-    if (smem > 200 * 1024) return QS_EUNSUPPORTED;
-    auto kern = quest_select_kernel<MT, D>;
-    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem))
-        return QS_ECUDA;
+    if (smem > 160 * 1024) return QS_EUNSUPPORTED;
+    constexpr int kRowsPerChunk = rows_per_chunk<MT, D>();
     const int chunks = max(1, (maxnb + kRowsPerChunk - 1) / kRowsPerChunk);
-    dim3 grid(chunks, a.B * a.N);
-    kern<<<grid, kThreads, smem, s>>>(a);
-    QS_CHECK_LAUNCH();
-    return QS_OK;
+    if (chunks == 1) return launch_mode<MT, D, kSingle>(a, chunks, smem, s);
+    if (chunks <= 8) return launch_mode<MT, D, kCluster>(a, chunks, smem, s);
+    return launch_mode<MT, D, kGlobal>(a, chunks, smem, s);
 }
 
 }  // namespace
@@ -248,7 +356,9 @@ qs_status block_select_impl(const void* q, qs_dtype q_dtype, const void* maxbloc
     if (q_dtype != QS_F32 && q_dtype != QS_BF16 && q_dtype != QS_F16) return QS_EDTYPE;
     if (meta_dtype != QS_F32 && meta_dtype != QS_BF16 && meta_dtype != QS_F16) return QS_EDTYPE;
     if (D != 64 && D != 128) return QS_EUNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(maxblocks) | reinterpret_cast<uintptr_t>(minblocks)) % 16)
+    if (H / N > kMaxG) return QS_EUNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(maxblocks) | reinterpret_cast<uintptr_t>(minblocks) |
+         reinterpret_cast<uintptr_t>(q)) % 16)
         return QS_EINVAL;
     if (t >= 0 && static_cast<long long>(k) < 2 + (static_cast<long long>(t) + BS - 1) / BS)
         return QS_EINVAL;  // the forced set may not fit
@@ -270,6 +380,7 @@ qs_status block_select_impl(const void* q, qs_dtype q_dtype, const void* maxbloc
     a.B = B; a.H = H; a.N = N; a.BS = BS; a.k = k; a.t = t;
     a.selected = selected;
     a.scores = scores_opt ? scores_opt : reinterpret_cast<float*>(ws);
+    a.scores_out = scores_opt != nullptr;
     a.counters = reinterpret_cast<uint32_t*>(ws + align_up(static_cast<size_t>(B) * N * maxnb * 4, 256));
     a.dev_status = dev_status;
     if (D == 128) {

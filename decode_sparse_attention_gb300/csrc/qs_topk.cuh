@@ -19,7 +19,7 @@ namespace qs {
 enum : uint8_t { kCand = 1, kPick = 2, kFixed = 4 };
 
 template <int NT> struct TopkScratch {
-    uint32_t hist[256];
+    uint32_t hist[2][256];   // double-buffered: one pass fills, the next is cleared
     int warp_sums[NT / 32 + 1];
     uint32_t prefix;
     int remaining;
@@ -62,12 +62,13 @@ QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
                           TopkScratch<NT>& s) {
     const int tid = threadIdx.x, lane = tid & 31;
     if (want <= 0) return;
+    for (int i = tid; i < 256; i += NT) s.hist[0][i] = 0;
+    __syncthreads();
     uint32_t prefix = 0, mask = 0;
     int remaining = want;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += NT) s.hist[i] = 0;
-        __syncthreads();
+        uint32_t* hist = s.hist[pass & 1];
         for (int base = 0; base < n; base += NT) {
             const int j = base + tid;
             bool ok = false;
@@ -80,8 +81,10 @@ QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
                 }
             }
             const unsigned peers = __match_any_sync(0xffffffffu, digit);
-            if (ok && lane == __ffs(peers) - 1) atomicAdd(&s.hist[digit], __popc(peers));
+            if (ok && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
         }
+        // the other buffer is idle during this pass: clear it for the next
+        for (int i = tid; i < 256; i += NT) s.hist[(pass + 1) & 1][i] = 0;
         __syncthreads();
         if (tid < 32) {
             // lane l owns digits 255-8l ... 248-8l (descending)
@@ -89,7 +92,7 @@ QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
             uint32_t sum = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                c[i] = s.hist[255 - 8 * lane - i];
+                c[i] = hist[255 - 8 * lane - i];
                 sum += c[i];
             }
             uint32_t incl = sum;
@@ -121,7 +124,6 @@ QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
         prefix = s.prefix;
         remaining = s.remaining;
         mask |= 0xffu << shift;
-        __syncthreads();
     }
     // prefix = T (the want-th largest key); take every key > T and the first
     // `remaining` keys == T in index order.
@@ -174,6 +176,272 @@ QS_DEVINL int count_flags(const uint8_t* flags, uint8_t bits, int n, TopkScratch
     int tot;
     block_exclusive_scan<NT>(c, s, &tot);
     return tot;
+}
+
+}  // namespace qs
+
+namespace qs {
+
+// ---------------------------------------------------------------------------
+// One-warp selection for up to 32*M keys (no block barriers).
+//
+// Keys are held lane-strided in registers: entry i of lane l is index
+// j = 32*i + l, so walking i upward visits the indices in ascending order.
+// ---------------------------------------------------------------------------
+
+template <int M> struct WarpKeys {
+    uint32_t key[M];
+    uint32_t cand;    // bit i: entry i is a candidate
+    uint32_t fixed;   // bit i: entry i is always emitted
+    uint32_t pick;    // bit i: entry i was picked
+};
+
+QS_DEVINL unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Marks (in w.pick) the `want` candidates with the largest keys, equal keys
+// by lower index.  Requires want <= number of candidates.  Radix selection by
+// bisection: each step fixes one bit of the threshold key T from the count
+// of candidates above it (one warp reduction per bit; the bits shared by the
+// largest and smallest candidate key are skipped).
+template <int M>
+QS_DEVINL void warp_topk(WarpKeys<M>& w, int want) {
+    w.pick = 0;
+    if (want <= 0) return;
+    uint32_t kmax = 0, kmin = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < M; ++i)
+        if (w.cand >> i & 1) {
+            kmax = max(kmax, w.key[i]);
+            kmin = min(kmin, w.key[i]);
+        }
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    const uint32_t diff = kmax ^ kmin;
+    const int top = diff ? 31 - __clz(diff) : -1;   // highest bit that differs
+    uint32_t prefix = top >= 31 ? 0u : (kmax >> (top + 1)) << (top + 1);
+    int remaining = want;
+    for (int bit = top; bit >= 0; --bit) {
+        const uint32_t trial = prefix | (1u << bit);
+        const uint32_t hi_mask = ~((1u << bit) - 1u);   // bits >= bit
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < M; ++i)
+            c += (w.cand >> i & 1) && ((w.key[i] & hi_mask) == trial);
+        const int tot = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+        if (tot >= remaining) prefix = trial;
+        else remaining -= tot;
+    }
+    // prefix = T; take every candidate above T and the first `remaining`
+    // equal to T in index order
+    const unsigned below = lanemask_lt();
+    int eq_seen = 0;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const bool c = w.cand >> i & 1;
+        const bool eq = c && w.key[i] == prefix;
+        const unsigned em = __ballot_sync(0xffffffffu, eq);
+        const int rank = eq_seen + __popc(em & below);
+        eq_seen += __popc(em);
+        if (c && (w.key[i] > prefix || (eq && rank < remaining))) w.pick |= 1u << i;
+    }
+}
+
+// Writes the indices of entries with (fixed | pick) in ascending order into
+// out[0..k), -1 padded.  Returns how many there are.
+template <int M>
+QS_DEVINL int warp_emit(const WarpKeys<M>& w, int k, int32_t* out) {
+    const int lane = threadIdx.x & 31;
+    const unsigned below = lanemask_lt();
+    int base = 0;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const bool e = ((w.fixed | w.pick) >> i) & 1;
+        const unsigned em = __ballot_sync(0xffffffffu, e);
+        const int pos = base + __popc(em & below);
+        if (e && pos < k) out[pos] = 32 * i + lane;
+        base += __popc(em);
+    }
+    for (int p = base + lane; p < k; p += 32) out[p] = -1;
+    return base;
+}
+
+}  // namespace qs
+
+namespace qs {
+
+// ---------------------------------------------------------------------------
+// Histogram top-k: one pass of a 256-bin histogram over the bits right
+// below the common prefix of the candidate keys finds the bin that holds the
+// want-th key; bins above it are taken whole and the few keys inside the
+// boundary bin are ranked exactly (key desc, index asc) by one warp.  Five
+// block barriers in the common case; falls back to the 4-pass radix
+// selection when the boundary bin holds more than kListMax keys.
+// ---------------------------------------------------------------------------
+
+constexpr int kHistBins = 256;
+constexpr int kListMax = 64;
+
+struct TopkFastScratch {
+    __align__(16) uint32_t hist[kHistBins];
+    uint32_t list_key[kListMax];
+    int list_idx[kListMax];
+    uint32_t wmax[32], wmin[32];
+    int wcnt[32];
+    int nlist, dstar, remaining, overflow;
+};
+
+// Clears the histogram; call before topk_fast with a barrier in between
+// (the scoring phase of the callers provides it).
+template <int NT>
+QS_DEVINL void topk_fast_clear(TopkFastScratch& s) {
+    for (int i = threadIdx.x; i < kHistBins; i += NT) s.hist[i] = 0;
+    if (threadIdx.x == 0) s.nlist = 0;
+}
+
+// Sets kPick on the top `want` entries among those flagged kCand (keys and
+// flags in shared memory).  Requires the histogram cleared beforehand.
+template <int NT>
+QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
+                         TopkFastScratch& s, TopkScratch<NT>& rs) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = NT / 32;
+    if (want <= 0) return;
+    // 0. candidate count and key range
+    uint32_t lmax = 0, lmin = 0xffffffffu;
+    int lc = 0;
+    for (int j = tid; j < n; j += NT)
+        if (flags[j] & kCand) {
+            const uint32_t k = keys[j];
+            lmax = max(lmax, k);
+            lmin = min(lmin, k);
+            ++lc;
+        }
+    lmax = __reduce_max_sync(0xffffffffu, lmax);
+    lmin = __reduce_min_sync(0xffffffffu, lmin);
+    lc = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(lc)));
+    if (lane == 0) {
+        s.wmax[warp] = lmax;
+        s.wmin[warp] = lmin;
+        s.wcnt[warp] = lc;
+    }
+    __syncthreads();
+    uint32_t kmax = 0, kmin = 0xffffffffu;
+    int ncand = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        kmax = max(kmax, s.wmax[w]);
+        kmin = min(kmin, s.wmin[w]);
+        ncand += s.wcnt[w];
+    }
+    if (want >= ncand) {          // everything goes
+        for (int j = tid; j < n; j += NT)
+            if (flags[j] & kCand) flags[j] |= kPick;
+        __syncthreads();
+        return;
+    }
+    const uint32_t diff = kmax ^ kmin;
+    const int top = diff ? 31 - __clz(diff) : 0;
+    const int lo = top >= 7 ? top - 7 : 0;
+    const int nbins = 1 << (top - lo + 1);
+    const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
+    // 1. histogram of the digit below the common prefix
+    for (int j = tid; j < n; j += NT)
+        if (flags[j] & kCand) atomicAdd(&s.hist[(keys[j] >> lo) & dmask], 1u);
+    __syncthreads();
+    // 2. boundary bin: one warp scans the 256 bins from the top, 8 per lane
+    //    (two 16-byte loads each)
+    if (warp == 0) {
+        const int d_hi = kHistBins - 1 - 8 * lane;          // lane's bins d_hi .. d_hi-7
+        const uint4 h0 = *reinterpret_cast<const uint4*>(&s.hist[d_hi - 7]);
+        const uint4 h1 = *reinterpret_cast<const uint4*>(&s.hist[d_hi - 3]);
+        const int cnt[8] = {static_cast<int>(h1.w), static_cast<int>(h1.z), static_cast<int>(h1.y),
+                            static_cast<int>(h1.x), static_cast<int>(h0.w), static_cast<int>(h0.z),
+                            static_cast<int>(h0.y), static_cast<int>(h0.x)};   // descending bins
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c += cnt[i];
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int excl = incl - c;
+        if (excl < want && incl >= want) {
+            int above = excl;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (above + cnt[i] >= want) {
+                    s.dstar = d_hi - i;
+                    s.remaining = want - above;
+                    break;
+                }
+                above += cnt[i];
+            }
+        }
+    }
+    __syncthreads();
+    const uint32_t dstar = static_cast<uint32_t>(s.dstar);
+    // 3. above the boundary: taken; inside: listed
+    for (int j = tid; j < n; j += NT)
+        if (flags[j] & kCand) {
+            const uint32_t d = (keys[j] >> lo) & dmask;
+            if (d > dstar) {
+                flags[j] |= kPick;
+            } else if (d == dstar) {
+                const int pos = atomicAdd(&s.nlist, 1);
+                if (pos < kListMax) {
+                    s.list_key[pos] = keys[j];
+                    s.list_idx[pos] = j;
+                }
+            }
+        }
+    __syncthreads();
+    const int nlist = s.nlist;
+    if (nlist <= kListMax) {
+        // 4. exact ranks inside the boundary bin
+        if (warp == 0) {
+            const int remaining = s.remaining;
+            for (int e = lane; e < nlist; e += 32) {
+                const uint32_t ke = s.list_key[e];
+                const int ie = s.list_idx[e];
+                int rank = 0;
+                for (int f = 0; f < nlist; ++f) {
+                    const uint32_t kf = s.list_key[f];
+                    rank += kf > ke || (kf == ke && s.list_idx[f] < ie);
+                }
+                if (rank < remaining) flags[ie] |= kPick;
+            }
+        }
+        __syncthreads();
+        return;
+    }
+    // a crowded boundary bin (many equal keys): exact radix selection
+    for (int j = tid; j < n; j += NT) flags[j] &= static_cast<uint8_t>(~kPick);
+    __syncthreads();
+    topk_flags<NT>(keys, flags, n, want, rs);
+}
+
+// One warp writes the indices j with (flags[j] & bits) in ascending order
+// into out[0..k), -1 padded; returns their number (in every lane).
+QS_DEVINL int warp_emit_flags(const uint8_t* flags, uint8_t bits, int n, int k, int32_t* out) {
+    const int lane = threadIdx.x & 31;
+    const unsigned below = lanemask_lt();
+    int base = 0;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        const int j = j0 + lane;
+        const bool e = j < n && (flags[j] & bits);
+        const unsigned em = __ballot_sync(0xffffffffu, e);
+        const int pos = base + __popc(em & below);
+        if (e && pos < k) out[pos] = j;
+        base += __popc(em);
+    }
+    for (int p = base + lane; p < k; p += 32) out[p] = -1;
+    return base;
 }
 
 }  // namespace qs
