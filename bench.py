@@ -219,7 +219,7 @@ def committed_traffic(workload: str):
 # our implementation
 # ---------------------------------------------------------------------------
 
-def setup(w, seed, dev):
+def setup(w, seed, dev, fused_select=-1):
     from decode_sparse_attention_gb300 import questsparse as qs
     x = synth.make(w, seed=seed, device=dev)
     mode = 0 if w.mode == "quest" else 1
@@ -249,7 +249,8 @@ def setup(w, seed, dev):
                                  metadata_block_tables=x["meta_block_tables"],
                                  tokens_since_metadata_update=x["t"],
                                  importance=x.get("importance"), n_probe=w.n_probe,
-                                 k_scale=x.get("k_scale"), v_scale=x.get("v_scale"))
+                                 k_scale=x.get("k_scale"), v_scale=x.get("v_scale"),
+                                 fused_select=fused_select)
     return x, mode, sel, out, params, meta_ms
 
 
@@ -285,7 +286,7 @@ def run_ours(args, w):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     qs.lib()
-    x, mode, sel, out, params, meta_ms = setup(w, args.seed + rank, dev)
+    x, mode, sel, out, params, meta_ms = setup(w, args.seed + rank, dev, args.fused_select)
     flush = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sink = torch.zeros((), dtype=torch.int64, device=dev)
     stream = torch.cuda.Stream(dev)
@@ -394,6 +395,8 @@ def run_ours(args, w):
             "parallelism": "replicas" if ws_ > 1 else "single GPU",
             "l2": "256 MiB written then read back between timed steps",
             "step": "qs_sparse_decode_step replayed as a CUDA graph",
+            "fused_select": args.fused_select,
+            "kernels_per_step": qs.step_kernels(params),
         },
         "step_gbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9, 1),
         "step_frac_of_peak": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / peak, 4),
@@ -417,7 +420,7 @@ def run_ours(args, w):
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": qs.step_kernels(params) * args.steps,
     }
     if meta_ms is not None:
         L = x["meta_seq_lens"].cpu().numpy()
@@ -562,6 +565,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-select", type=int, default=-1, choices=[-1, 0, 1],
+                    help="Quest step: -1 library's choice, 0 selector + attention kernels, "
+                         "1 the fused one-kernel step")
     ap.add_argument("--preroll-s", type=float, default=1.5,
                     help="seconds of back-to-back steps before the timed loop (clock sampling)")
     args = ap.parse_args(argv)

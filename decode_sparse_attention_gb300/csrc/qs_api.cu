@@ -161,6 +161,9 @@ extern "C" qs_status qs_sparse_decode_step(const qs_step_params* p, qs_stream_t 
         sel_ws = align_up(select_workspace_bytes(p->B, p->N, p->MMBPR * p->BS), 256);
         sel_heads = p->N;
         if (!ws || p->workspace_bytes < sel_ws) return QS_EWORKSPACE;
+        bool fused = false;
+        st = quest_step_fused(p, ws + sel_ws, p->workspace_bytes - sel_ws, s, &fused, true);
+        if (fused) return st;
         st = block_select_impl(p->q, p->q_dtype, p->maxblocks, p->minblocks, p->kv_dtype,
                                p->meta_block_tables, p->MMBPR, p->num_meta_blocks, p->seq_lens,
                                p->B, p->H, p->N, p->D, p->BS, p->k,
@@ -183,4 +186,19 @@ extern "C" qs_status qs_sparse_decode_step(const qs_step_params* p, qs_stream_t 
                             p->selected, sel_heads, p->k, p->softmax_scale, p->B, p->H, p->N, p->D,
                             p->BS, p->out, p->lse_opt, ws + sel_ws, p->workspace_bytes - sel_ws,
                             p->dev_status, s, /*pdl=*/true);
+}
+
+extern "C" qs_status qs_step_kernels(const qs_step_params* p, int32_t* kernels) {
+    using namespace qs;
+    if (!p || !kernels) return QS_EINVAL;
+    *kernels = 2;
+    if (p->mode != 0) return QS_OK;
+    if (p->MMBPR < 0 || p->BS <= 0) return QS_EINVAL;
+    const size_t sel_ws = align_up(select_workspace_bytes(p->B, p->N, p->MMBPR * p->BS), 256);
+    if (!p->workspace || p->workspace_bytes < sel_ws) return QS_EWORKSPACE;
+    bool fused = false;
+    quest_step_fused(p, static_cast<uint8_t*>(p->workspace) + sel_ws, p->workspace_bytes - sel_ws,
+                     nullptr, &fused, false);
+    if (fused) *kernels = 1;
+    return QS_OK;
 }

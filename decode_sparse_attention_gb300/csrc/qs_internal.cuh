@@ -37,4 +37,12 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
                            cudaStream_t stream, bool pdl);
 
+// Fused Quest decode step (one kernel).  Sets *taken = false, and enqueues
+// nothing, when the sizes are outside what the fused kernel serves or the
+// inputs would make either kernel of the two-kernel step report an error;
+// the caller then runs the two-kernel step.  attn_ws: the attention part of
+// the step's workspace.  launch = false only decides (*taken).
+qs_status quest_step_fused(const qs_step_params* p, void* attn_ws, size_t attn_ws_bytes,
+                           cudaStream_t stream, bool* taken, bool launch);
+
 }  // namespace qs

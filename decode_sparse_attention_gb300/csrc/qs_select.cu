@@ -21,6 +21,7 @@
 #include <cooperative_groups.h>
 
 #include "qs_internal.cuh"
+#include "qs_quest_score.cuh"
 #include "qs_topk.cuh"
 
 namespace qs {
@@ -50,78 +51,6 @@ struct SelectArgs {
     uint32_t* counters;   // [B*N]
     int32_t* dev_status;
 };
-
-// Partial score of one 16-byte chunk of a max row and a min row against the
-// matching fp32 query channels.
-template <Dt T> struct RowChunk;
-
-template <> struct RowChunk<Dt::F32> {
-    static constexpr int kElems = 4;
-    static QS_DEVINL float dot(const float* qg, uint4 mx, uint4 mn) {
-        const uint32_t a[4] = {mx.x, mx.y, mx.z, mx.w};
-        const uint32_t c[4] = {mn.x, mn.y, mn.z, mn.w};
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float p1 = qg[i] * __uint_as_float(a[i]);
-            const float p2 = qg[i] * __uint_as_float(c[i]);
-            s += fmaxf(p1, p2);
-        }
-        return s;
-    }
-};
-
-template <Dt T> struct RowChunk16 {
-    static constexpr int kElems = 8;
-    static QS_DEVINL float dot(const float* qg, uint4 mx, uint4 mn) {
-        const uint32_t a[4] = {mx.x, mx.y, mx.z, mx.w};
-        const uint32_t c[4] = {mn.x, mn.y, mn.z, mn.w};
-        unsigned long long acc = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 fa = pair_to_float2<T>(a[i]);
-            const float2 fc = pair_to_float2<T>(c[i]);
-            const unsigned long long q2 = pack2(qg[2 * i], qg[2 * i + 1]);
-            const float2 p1 = unpack2(mul2(q2, pack2(fa.x, fa.y)));
-            const float2 p2 = unpack2(mul2(q2, pack2(fc.x, fc.y)));
-            const float2 m = make_float2(fmaxf(p1.x, p2.x), fmaxf(p1.y, p2.y));
-            acc = fma2(pack2(1.f, 1.f), pack2(m.x, m.y), acc);
-        }
-        const float2 r = unpack2(acc);
-        return r.x + r.y;
-    }
-};
-template <> struct RowChunk<Dt::BF16> : RowChunk16<Dt::BF16> {};
-template <> struct RowChunk<Dt::F16> : RowChunk16<Dt::F16> {};
-
-// kEl query elements of one head starting at element `off`, as fp32.
-template <int kEl>
-QS_DEVINL void load_q_slice(const void* q, int q_dt, size_t off, float (&out)[kEl]) {
-    if (q_dt == QS_F32) {
-        const float* p = static_cast<const float*>(q) + off;
-#pragma unroll
-        for (int e = 0; e < kEl; e += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(p + e);
-            out[e] = v.x; out[e + 1] = v.y; out[e + 2] = v.z; out[e + 3] = v.w;
-        }
-    } else {
-        const uint16_t* p = static_cast<const uint16_t*>(q) + off;
-        uint32_t w[kEl / 2];
-        if constexpr (kEl == 8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(p);
-            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-        } else {
-            const uint2 v = *reinterpret_cast<const uint2*>(p);
-            w[0] = v.x; w[1] = v.y;
-        }
-#pragma unroll
-        for (int i = 0; i < kEl / 2; ++i) {
-            const float2 f = q_dt == QS_BF16 ? pair_to_float2<Dt::BF16>(w[i]) : pair_to_float2<Dt::F16>(w[i]);
-            out[2 * i] = f.x;
-            out[2 * i + 1] = f.y;
-        }
-    }
-}
 
 enum Mode : int { kSingle = 0, kCluster = 1, kGlobal = 2 };
 
@@ -251,9 +180,7 @@ __global__ void __launch_bounds__(kThreads, 2) quest_select_kernel(SelectArgs a)
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
         const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
-        float s = RowChunk<MT>::dot(qreg, vmx[r], vmn[r]);
-#pragma unroll
-        for (int o = kLanesPerRow / 2; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        const float s = row_score_reduce<kLanesPerRow>(RowChunk<MT>::dot(qreg, vmx[r], vmn[r]));
         if (cl == 0 && j < j_end) {
             const float v = live[r] ? s : __int_as_float(0xff800000);
             if (MODE != kGlobal) dst_keys[j] = float_key(v);
@@ -280,12 +207,8 @@ __global__ void __launch_bounds__(kThreads, 2) quest_select_kernel(SelectArgs a)
     }
 
     // step 2.3 + window
-    int w0 = nb;  // first window block (nb: none)
-    if (a.t >= 0 && nb > 0) {
-        w0 = L - a.t >= 0 ? (L - a.t) / BS : 0;
-        w0 = min(w0, nb - 1);
-    }
-    const int n_forced = a.t >= 0 && nb > 0 ? (nb - w0) + (w0 > 0 ? 1 : 0) : 0;
+    const int w0 = forced_window_start(L, BS, nb, a.t);   // nb: no window
+    const int n_forced = forced_count(nb, w0, a.t);
     if (n_forced > a.k) {
         if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_EFORCED);
         for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;

@@ -10,6 +10,9 @@
 // every candidate key > T plus the first keys == T in index order (a
 // CTA-wide prefix count).  The result is a set, returned as flags, so the
 // cost is independent of k.
+//
+// Every routine runs on all threads of the block (blockDim.x, a multiple of
+// 32, at most NT: the template argument only sizes the scratch).
 #pragma once
 
 #include "qs_common.cuh"
@@ -31,6 +34,7 @@ template <int NT> struct TopkScratch {
 template <int NT>
 QS_DEVINL int block_exclusive_scan(int v, TopkScratch<NT>& s, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nw = static_cast<int>(blockDim.x) >> 5;
     int x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -40,17 +44,17 @@ QS_DEVINL int block_exclusive_scan(int v, TopkScratch<NT>& s, int* total) {
     if (lane == 31) s.warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int w = lane < NT / 32 ? s.warp_sums[lane] : 0;
+        int w = lane < nw ? s.warp_sums[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
-        if (lane < NT / 32) s.warp_sums[lane] = w;
+        if (lane < nw) s.warp_sums[lane] = w;
     }
     __syncthreads();
     const int before = warp ? s.warp_sums[warp - 1] : 0;
-    *total = s.warp_sums[NT / 32 - 1];
+    *total = s.warp_sums[nw - 1];
     __syncthreads();
     return before + x - v;
 }
@@ -61,15 +65,16 @@ template <int NT>
 QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
                           TopkScratch<NT>& s) {
     const int tid = threadIdx.x, lane = tid & 31;
+    const int nt = static_cast<int>(blockDim.x);
     if (want <= 0) return;
-    for (int i = tid; i < 256; i += NT) s.hist[0][i] = 0;
+    for (int i = tid; i < 256; i += nt) s.hist[0][i] = 0;
     __syncthreads();
     uint32_t prefix = 0, mask = 0;
     int remaining = want;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         uint32_t* hist = s.hist[pass & 1];
-        for (int base = 0; base < n; base += NT) {
+        for (int base = 0; base < n; base += nt) {
             const int j = base + tid;
             bool ok = false;
             uint32_t digit = 0x100u + lane;
@@ -84,7 +89,7 @@ QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
             if (ok && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
         }
         // the other buffer is idle during this pass: clear it for the next
-        for (int i = tid; i < 256; i += NT) s.hist[(pass + 1) & 1][i] = 0;
+        for (int i = tid; i < 256; i += nt) s.hist[(pass + 1) & 1][i] = 0;
         __syncthreads();
         if (tid < 32) {
             // lane l owns digits 255-8l ... 248-8l (descending)
@@ -127,7 +132,7 @@ QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
     }
     // prefix = T (the want-th largest key); take every key > T and the first
     // `remaining` keys == T in index order.
-    const int per = (n + NT - 1) / NT;
+    const int per = (n + nt - 1) / nt;
     const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
     int eq = 0;
     for (int j = j0; j < j1; ++j) eq += (flags[j] & kCand) && keys[j] == prefix;
@@ -146,132 +151,11 @@ QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
     __syncthreads();
 }
 
-// Writes the indices j with (flags[j] & bits) != 0 in ascending order into
-// out[0..k), padding with -1; at most k indices are written.  Returns the
-// number of flagged entries (same value in every thread).
-template <int NT>
-QS_DEVINL int emit_sorted(const uint8_t* flags, uint8_t bits, int n, int k, int32_t* out,
-                          TopkScratch<NT>& s) {
-    const int tid = threadIdx.x;
-    const int per = (n + NT - 1) / NT;
-    const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
-    int c = 0;
-    for (int j = j0; j < j1; ++j) c += (flags[j] & bits) != 0;
-    int tot;
-    int pos = block_exclusive_scan<NT>(c, s, &tot);
-    for (int j = j0; j < j1; ++j)
-        if (flags[j] & bits) {
-            if (pos < k) out[pos] = j;
-            ++pos;
-        }
-    for (int i = tot + tid; i < k; i += NT) out[i] = -1;
-    return tot;
-}
-
-// Number of entries with (flags & bits) != 0 (same value in every thread).
-template <int NT>
-QS_DEVINL int count_flags(const uint8_t* flags, uint8_t bits, int n, TopkScratch<NT>& s) {
-    int c = 0;
-    for (int j = threadIdx.x; j < n; j += NT) c += (flags[j] & bits) != 0;
-    int tot;
-    block_exclusive_scan<NT>(c, s, &tot);
-    return tot;
-}
-
-}  // namespace qs
-
-namespace qs {
-
-// ---------------------------------------------------------------------------
-// One-warp selection for up to 32*M keys (no block barriers).
-//
-// Keys are held lane-strided in registers: entry i of lane l is index
-// j = 32*i + l, so walking i upward visits the indices in ascending order.
-// ---------------------------------------------------------------------------
-
-template <int M> struct WarpKeys {
-    uint32_t key[M];
-    uint32_t cand;    // bit i: entry i is a candidate
-    uint32_t fixed;   // bit i: entry i is always emitted
-    uint32_t pick;    // bit i: entry i was picked
-};
-
 QS_DEVINL unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
 }
-
-// Marks (in w.pick) the `want` candidates with the largest keys, equal keys
-// by lower index.  Requires want <= number of candidates.  Radix selection by
-// bisection: each step fixes one bit of the threshold key T from the count
-// of candidates above it (one warp reduction per bit; the bits shared by the
-// largest and smallest candidate key are skipped).
-template <int M>
-QS_DEVINL void warp_topk(WarpKeys<M>& w, int want) {
-    w.pick = 0;
-    if (want <= 0) return;
-    uint32_t kmax = 0, kmin = 0xffffffffu;
-#pragma unroll
-    for (int i = 0; i < M; ++i)
-        if (w.cand >> i & 1) {
-            kmax = max(kmax, w.key[i]);
-            kmin = min(kmin, w.key[i]);
-        }
-    kmax = __reduce_max_sync(0xffffffffu, kmax);
-    kmin = __reduce_min_sync(0xffffffffu, kmin);
-    const uint32_t diff = kmax ^ kmin;
-    const int top = diff ? 31 - __clz(diff) : -1;   // highest bit that differs
-    uint32_t prefix = top >= 31 ? 0u : (kmax >> (top + 1)) << (top + 1);
-    int remaining = want;
-    for (int bit = top; bit >= 0; --bit) {
-        const uint32_t trial = prefix | (1u << bit);
-        const uint32_t hi_mask = ~((1u << bit) - 1u);   // bits >= bit
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < M; ++i)
-            c += (w.cand >> i & 1) && ((w.key[i] & hi_mask) == trial);
-        const int tot = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
-        if (tot >= remaining) prefix = trial;
-        else remaining -= tot;
-    }
-    // prefix = T; take every candidate above T and the first `remaining`
-    // equal to T in index order
-    const unsigned below = lanemask_lt();
-    int eq_seen = 0;
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-        const bool c = w.cand >> i & 1;
-        const bool eq = c && w.key[i] == prefix;
-        const unsigned em = __ballot_sync(0xffffffffu, eq);
-        const int rank = eq_seen + __popc(em & below);
-        eq_seen += __popc(em);
-        if (c && (w.key[i] > prefix || (eq && rank < remaining))) w.pick |= 1u << i;
-    }
-}
-
-// Writes the indices of entries with (fixed | pick) in ascending order into
-// out[0..k), -1 padded.  Returns how many there are.
-template <int M>
-QS_DEVINL int warp_emit(const WarpKeys<M>& w, int k, int32_t* out) {
-    const int lane = threadIdx.x & 31;
-    const unsigned below = lanemask_lt();
-    int base = 0;
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-        const bool e = ((w.fixed | w.pick) >> i) & 1;
-        const unsigned em = __ballot_sync(0xffffffffu, e);
-        const int pos = base + __popc(em & below);
-        if (e && pos < k) out[pos] = 32 * i + lane;
-        base += __popc(em);
-    }
-    for (int p = base + lane; p < k; p += 32) out[p] = -1;
-    return base;
-}
-
-}  // namespace qs
-
-namespace qs {
 
 // ---------------------------------------------------------------------------
 // Histogram top-k: one pass of a 256-bin histogram over the bits right
@@ -298,7 +182,7 @@ struct TopkFastScratch {
 // (the scoring phase of the callers provides it).
 template <int NT>
 QS_DEVINL void topk_fast_clear(TopkFastScratch& s) {
-    for (int i = threadIdx.x; i < kHistBins; i += NT) s.hist[i] = 0;
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) s.hist[i] = 0;
     if (threadIdx.x == 0) s.nlist = 0;
 }
 
@@ -308,12 +192,12 @@ template <int NT>
 QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
                          TopkFastScratch& s, TopkScratch<NT>& rs) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NW = NT / 32;
+    const int NT_ = static_cast<int>(blockDim.x), NW = NT_ >> 5;   // NT_ <= NT
     if (want <= 0) return;
     // 0. candidate count and key range
     uint32_t lmax = 0, lmin = 0xffffffffu;
     int lc = 0;
-    for (int j = tid; j < n; j += NT)
+    for (int j = tid; j < n; j += NT_)
         if (flags[j] & kCand) {
             const uint32_t k = keys[j];
             lmax = max(lmax, k);
@@ -331,14 +215,13 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
     __syncthreads();
     uint32_t kmax = 0, kmin = 0xffffffffu;
     int ncand = 0;
-#pragma unroll
     for (int w = 0; w < NW; ++w) {
         kmax = max(kmax, s.wmax[w]);
         kmin = min(kmin, s.wmin[w]);
         ncand += s.wcnt[w];
     }
     if (want >= ncand) {          // everything goes
-        for (int j = tid; j < n; j += NT)
+        for (int j = tid; j < n; j += NT_)
             if (flags[j] & kCand) flags[j] |= kPick;
         __syncthreads();
         return;
@@ -349,7 +232,7 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
     const int nbins = 1 << (top - lo + 1);
     const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
     // 1. histogram of the digit below the common prefix
-    for (int j = tid; j < n; j += NT)
+    for (int j = tid; j < n; j += NT_)
         if (flags[j] & kCand) atomicAdd(&s.hist[(keys[j] >> lo) & dmask], 1u);
     __syncthreads();
     // 2. boundary bin: one warp scans the 256 bins from the top, 8 per lane
@@ -387,7 +270,7 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
     __syncthreads();
     const uint32_t dstar = static_cast<uint32_t>(s.dstar);
     // 3. above the boundary: taken; inside: listed
-    for (int j = tid; j < n; j += NT)
+    for (int j = tid; j < n; j += NT_)
         if (flags[j] & kCand) {
             const uint32_t d = (keys[j] >> lo) & dmask;
             if (d > dstar) {
@@ -421,7 +304,7 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
         return;
     }
     // a crowded boundary bin (many equal keys): exact radix selection
-    for (int j = tid; j < n; j += NT) flags[j] &= static_cast<uint8_t>(~kPick);
+    for (int j = tid; j < n; j += NT_) flags[j] &= static_cast<uint8_t>(~kPick);
     __syncthreads();
     topk_flags<NT>(keys, flags, n, want, rs);
 }
@@ -442,6 +325,157 @@ QS_DEVINL int warp_emit_flags(const uint8_t* flags, uint8_t bits, int n, int k, 
     }
     for (int p = base + lane; p < k; p += 32) out[p] = -1;
     return base;
+}
+
+}  // namespace qs
+
+namespace qs {
+
+// ---------------------------------------------------------------------------
+// One-warp top-k over keys in shared memory (no block barriers, so several
+// warps can select for different units at once).  Same order as above: key
+// descending, equal keys by lower index.  MSB-first radix selection with
+// 8-bit digits below the candidates' common prefix: a warp-private 256-bin
+// histogram finds the digit holding the want-th key; digits above it are
+// taken; the boundary digit is refined with the next 8 bits until at most
+// kWarpListMax keys remain in it, which are then ranked exactly (or, once
+// all 32 bits are fixed, the remaining equal keys are taken in index order).
+// ---------------------------------------------------------------------------
+
+constexpr int kWarpListMax = 64;
+
+struct WarpTopkScratch {
+    __align__(16) uint32_t hist[kHistBins];
+    uint32_t list_key[kWarpListMax];
+    int list_idx[kWarpListMax];
+};
+
+// Sets kPick on the top `want` entries among those flagged kCand; called by
+// all 32 lanes of one warp.
+QS_DEVINL void warp_topk_smem(const uint32_t* keys, uint8_t* flags, int n, int want,
+                              WarpTopkScratch& w) {
+    const int lane = threadIdx.x & 31;
+    const unsigned below = lanemask_lt();
+    if (want <= 0) return;
+    uint32_t kmax = 0, kmin = 0xffffffffu;
+    int c = 0;
+    for (int j = lane; j < n; j += 32)
+        if (flags[j] & kCand) {
+            const uint32_t k = keys[j];
+            kmax = max(kmax, k);
+            kmin = min(kmin, k);
+            ++c;
+        }
+    kmax = __reduce_max_sync(0xffffffffu, kmax);
+    kmin = __reduce_min_sync(0xffffffffu, kmin);
+    c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+    if (want >= c) {
+        for (int j = lane; j < n; j += 32)
+            if (flags[j] & kCand) flags[j] |= kPick;
+        __syncwarp();
+        return;
+    }
+    // keys still in play: candidates whose bits under pmask equal prefix
+    const uint32_t diff = kmax ^ kmin;
+    int hi = diff ? 31 - __clz(diff) : -1;            // highest bit not yet fixed
+    uint32_t pmask = hi >= 31 ? 0u : ~((2u << hi) - 1u);
+    uint32_t prefix = kmax & pmask;
+    int remaining = want;
+    while (hi >= 0) {
+        const int lo = hi >= 7 ? hi - 7 : 0;
+        const uint32_t dmask = (2u << (hi - lo)) - 1u;
+        for (int i = lane; i < kHistBins; i += 32) w.hist[i] = 0;
+        __syncwarp();
+        for (int j = lane; j < n; j += 32)
+            if ((flags[j] & kCand) && (keys[j] & pmask) == prefix)
+                atomicAdd(&w.hist[(keys[j] >> lo) & dmask], 1u);
+        __syncwarp();
+        // boundary digit: lane l sums digits 255-8l .. 248-8l (descending)
+        const int d_hi = kHistBins - 1 - 8 * lane;
+        const uint4 h0 = *reinterpret_cast<const uint4*>(&w.hist[d_hi - 7]);
+        const uint4 h1 = *reinterpret_cast<const uint4*>(&w.hist[d_hi - 3]);
+        const int cnt[8] = {static_cast<int>(h1.w), static_cast<int>(h1.z), static_cast<int>(h1.y),
+                            static_cast<int>(h1.x), static_cast<int>(h0.w), static_cast<int>(h0.z),
+                            static_cast<int>(h0.y), static_cast<int>(h0.x)};
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum += cnt[i];
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int excl = incl - sum;
+        int dsel = -1, above = 0, inbin = 0;
+        if (excl < remaining && incl >= remaining) {
+            int acc = excl;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (dsel < 0 && acc + cnt[i] >= remaining) {
+                    dsel = d_hi - i;
+                    above = acc;
+                    inbin = cnt[i];
+                }
+                if (dsel < 0) acc += cnt[i];
+            }
+        }
+        const unsigned who = __ballot_sync(0xffffffffu, dsel >= 0);
+        const int src = __ffs(who) - 1;
+        const uint32_t dstar = static_cast<uint32_t>(__shfl_sync(0xffffffffu, dsel, src));
+        above = __shfl_sync(0xffffffffu, above, src);
+        inbin = __shfl_sync(0xffffffffu, inbin, src);
+        // digits above the boundary are taken
+        for (int j = lane; j < n; j += 32)
+            if ((flags[j] & kCand) && (keys[j] & pmask) == prefix && ((keys[j] >> lo) & dmask) > dstar)
+                flags[j] |= kPick;
+        remaining -= above;
+        prefix |= dstar << lo;
+        pmask |= dmask << lo;
+        if (inbin == remaining) {          // the whole boundary digit goes
+            for (int j = lane; j < n; j += 32)
+                if ((flags[j] & kCand) && (keys[j] & pmask) == prefix) flags[j] |= kPick;
+            __syncwarp();
+            return;
+        }
+        if (inbin <= kWarpListMax) {       // rank the few keys left exactly
+            int base = 0;
+            for (int j0 = 0; j0 < n; j0 += 32) {
+                const int j = j0 + lane;
+                const bool in = j < n && (flags[j] & kCand) && (keys[j] & pmask) == prefix;
+                const unsigned m = __ballot_sync(0xffffffffu, in);
+                if (in) {
+                    const int pos = base + __popc(m & below);
+                    w.list_key[pos] = keys[j];
+                    w.list_idx[pos] = j;
+                }
+                base += __popc(m);
+            }
+            __syncwarp();
+            for (int e = lane; e < inbin; e += 32) {
+                const uint32_t ke = w.list_key[e];
+                int rank = 0;
+                for (int f = 0; f < inbin; ++f) {
+                    const uint32_t kf = w.list_key[f];
+                    rank += kf > ke || (kf == ke && f < e);   // the list is in index order
+                }
+                if (rank < remaining) flags[w.list_idx[e]] |= kPick;
+            }
+            __syncwarp();
+            return;
+        }
+        hi = lo - 1;
+    }
+    // every bit fixed: the keys in play are equal; take the lowest indices
+    int taken = 0;
+    for (int j0 = 0; j0 < n && taken < remaining; j0 += 32) {
+        const int j = j0 + lane;
+        const bool in = j < n && (flags[j] & kCand) && keys[j] == prefix;
+        const unsigned m = __ballot_sync(0xffffffffu, in);
+        if (in && taken + __popc(m & below) < remaining) flags[j] |= kPick;
+        taken += __popc(m);
+    }
+    __syncwarp();
 }
 
 }  // namespace qs

@@ -49,6 +49,7 @@ class StepParams(ctypes.Structure):
         ("softmax_scale", F),
         ("selected", P), ("out", P), ("lse_opt", P),
         ("workspace", P), ("workspace_bytes", SZ), ("dev_status", P),
+        ("fused_select", I32),
     ]
 
 
@@ -77,6 +78,7 @@ def lib():
                                                 I32, F, I32, I32, I32, I32, I32, P, P, P, SZ, P,
                                                 P]
             L.qs_sparse_decode_step.argtypes = [ctypes.POINTER(StepParams), P]
+            L.qs_step_kernels.argtypes = [ctypes.POINTER(StepParams), P]
             for f in ("qs_read_status", "qs_workspace_size", "qs_prefill_metadata",
                       "qs_block_select_paged", "qs_probe_select", "qs_sparse_decode_attn",
                       "qs_sparse_decode_step"):
@@ -319,9 +321,13 @@ def sparse_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, selected, so
 def make_step_params(mode, q, k_cache, v_cache, block_tables, seq_lens, k, selected, out,
                      ws, softmax_scale=None, maxblocks=None, minblocks=None,
                      metadata_block_tables=None, tokens_since_metadata_update=-1,
-                     importance=None, n_probe=8, k_scale=None, v_scale=None, lse=None):
+                     importance=None, n_probe=8, k_scale=None, v_scale=None, lse=None,
+                     fused_select=-1):
     """Fills a qs_step_params for qs_sparse_decode_step (pointers are captured;
-    keep the tensors alive while the params are in use)."""
+    keep the tensors alive while the params are in use).  fused_select (Quest
+    mode): -1 lets the library choose between the fused one-kernel step and
+    the selector + attention pair, 0 forces the pair, 1 the fused kernel
+    whenever the sizes fit it."""
     B, H, D = q.shape
     P_, BS, N, _ = k_cache.shape
     p = StepParams()
@@ -350,6 +356,7 @@ def make_step_params(mode, q, k_cache, v_cache, block_tables, seq_lens, k, selec
     p.lse_opt = lse.data_ptr() if lse is not None else None
     p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
     p.dev_status = status_word(q.device).data_ptr()
+    p.fused_select = int(fused_select)
     return p
 
 
@@ -357,6 +364,14 @@ def step_workspace_bytes(mode, B, H, N, D, BS, k, MMBPR=0, MKBPR=0):
     if mode == 0:
         return workspace_size(OP_STEP_QUEST, B, H, N, D, BS, k, MMBPR * BS, N)
     return workspace_size(OP_STEP_PROBE, B, H, N, D, BS, k, MKBPR, H)
+
+
+def step_kernels(params: StepParams) -> int:
+    """Number of kernels one qs_sparse_decode_step(params) launches (1: the
+    fused Quest kernel, 2: selector + attention)."""
+    n = I32(0)
+    _check(lib().qs_step_kernels(ctypes.byref(params), ctypes.byref(n)), "qs_step_kernels")
+    return int(n.value)
 
 
 def sparse_decode_step(params: StepParams, device=None):

@@ -228,11 +228,23 @@ qs_status qs_sparse_decode_attn_noalloc(const void* q, qs_dtype q_dtype, const v
                                         int32_t D, int32_t BS, float* out, float* lse_opt,
                                         int32_t* dev_status, qs_stream_t stream);
 
-/* One decode step: a selector followed by the attention, enqueued back to back
- * on one stream (the attention is launched as a programmatic dependent of the
- * selector).  Quest mode reads maxblocks/minblocks/meta tables and writes
- * selected [B, N, k]; probe mode reads importance and writes selected [B, H, k].
- * The workspace is shared: size it with QS_OP_DECODE_STEP_QUEST/_PROBE. */
+/* One decode step: block selection followed by the sparse attention.  Quest
+ * mode reads maxblocks/minblocks/meta tables and writes selected [B, N, k];
+ * probe mode reads importance and writes selected [B, H, k].  The workspace is
+ * shared: size it with QS_OP_DECODE_STEP_QUEST/_PROBE.
+ *
+ * Quest mode can run as ONE fused kernel: every CTA selects the (request, KV
+ * head) units its share of the attention touches and streams their K/V at
+ * once, with no hand-off between CTAs (a unit split between two CTAs is
+ * selected by both, identically).  Otherwise -- and always in probe mode --
+ * the selector and the attention run as two kernels on the stream, the
+ * attention launched as a programmatic dependent of the selector.
+ * Both forms give the same selection and the same attention output, and
+ * report the same device-side errors.  fused_select: -1 = the library's
+ * choice (currently always two kernels: on GB300 the fused kernel measured
+ * slower at every benchmark shape, because each CTA's K/V stream waits for
+ * its own metadata scan and top-k), 0 = two kernels, 1 = the fused kernel
+ * whenever the sizes fit its shared memory. */
 typedef struct {
     int32_t mode;                    /* 0 = Quest, 1 = probe/importance        */
     const void* q; qs_dtype q_dtype;
@@ -254,9 +266,16 @@ typedef struct {
     int32_t* selected; float* out; float* lse_opt;
     void* workspace; size_t workspace_bytes;
     int32_t* dev_status;
+    int32_t fused_select;            /* Quest mode: -1 auto, 0 off, 1 on     */
 } qs_step_params;
 
 qs_status qs_sparse_decode_step(const qs_step_params* params, qs_stream_t stream);
+
+/* How many kernels qs_sparse_decode_step(params) launches: 1 when it takes the
+ * fused Quest kernel, else 2 (selector + attention).  Enqueues nothing and
+ * reads no device memory.  Returns QS_EINVAL for a NULL argument,
+ * QS_EWORKSPACE when the workspace is too small to hold the selector part. */
+qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
 
 #ifdef __cplusplus
 }

@@ -90,3 +90,18 @@ def test_step_params_layout_matches_header():
             c_fields.append(nm.strip().lstrip("*").strip())
     py_fields = [f[0] for f in qs.StepParams._fields_]
     assert py_fields == c_fields
+
+
+def test_step_kernels_query_without_gpu(built_lib):
+    """qs_step_kernels decides without touching the device: probe mode and
+    fused_select = 0 always run two kernels; a NULL argument is rejected."""
+    from decode_sparse_attention_gb300 import questsparse as qs
+    p = qs.StepParams()
+    p.mode, p.B, p.H, p.N, p.D, p.BS, p.k = 1, 1, 16, 8, 128, 32, 32
+    assert qs.step_kernels(p) == 2
+    ws = (ctypes.c_uint8 * 1024)()
+    p.mode, p.MMBPR, p.fused_select = 0, 1, 0
+    p.workspace, p.workspace_bytes = ctypes.addressof(ws), 1 << 40
+    assert qs.step_kernels(p) == 2
+    n = ctypes.c_int32(0)
+    assert built_lib.qs_step_kernels(None, ctypes.byref(n)) == 1       # QS_EINVAL
