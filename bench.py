@@ -5,12 +5,17 @@ probe/importance selector) followed by the split-K sparse attention, enqueued
 through the C ABI (qs_sparse_decode_step) and replayed as a CUDA graph.  The
 metadata prefill is set-up, timed separately and reported on its own.
 
-Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream, with a 256 MiB write between steps so that no input of a
-step is served from the 129 MB L2.  The dominant kernel (the attention) is
-also timed alone the same way for the roofline.  Under torchrun every rank
-runs an independent replica (the path needs no collective) and the slowest
-rank's time is reported.
+Timing: the step is captured as a CUDA graph for each of R input sets
+(same shapes and lengths, other seeds), R chosen so that one rotation moves
+more than 3x the 129 MB L2; W warm-up steps, then K steps replayed back to
+back in rotation, each set's inputs evicted from L2 by the others' traffic
+before its next turn.  value = the span of the K steps on the launching
+stream's CUDA events / K.  Workloads too small for a rotation of at most
+--max-sets sets are timed one step at a time with a 256 MiB L2 flush before
+each.  The dominant kernel (the attention) and the selector are timed alone
+the same way; a flushed one-step time is reported beside the value.  Under
+torchrun every rank runs an independent replica (the path needs no
+collective) and the slowest rank's time is reported.
 
 JSON line keys: metric, value (us per step, lower is better), unit, roofline
 (attention kernel vs the measured HBM copy bandwidth), cpu_baseline (the
@@ -219,9 +224,9 @@ def committed_traffic(workload: str):
 # our implementation
 # ---------------------------------------------------------------------------
 
-def setup(w, seed, dev, fused_select=-1):
+def setup(w, seed, dev, fused_select=-1, seq_lens=None):
     from decode_sparse_attention_gb300 import questsparse as qs
-    x = synth.make(w, seed=seed, device=dev)
+    x = synth.make(w, seed=seed, device=dev, seq_lens=seq_lens)
     mode = 0 if w.mode == "quest" else 1
     meta_ms = None
     if mode == 0:
@@ -263,8 +268,8 @@ def flush_l2(flush, sink):
 
 
 def timed_graph(graph, flush, sink, steps, stream):
-    """Per-step CUDA-event durations (ms) of graph replays with an L2 flush
-    between steps."""
+    """Per-step CUDA-event durations (ms) of replays of one graph with an L2
+    flush between steps (each replay bracketed by its own events)."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
     with torch.cuda.stream(stream):     # flush, replay and both events on one stream
@@ -277,6 +282,39 @@ def timed_graph(graph, flush, sink, steps, stream):
     return [s.elapsed_time(e) for s, e in evs]
 
 
+def timed_rotation(graphs, steps, stream):
+    """Back-to-back replays cycling through the graphs of R input sets (the
+    other R-1 sets' traffic evicts a set's inputs from L2 before its next
+    turn).  Returns the per-step intervals between consecutive events (ms)
+    and the whole span (ms) from the first event to the last."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    iv = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    return iv, evs[0].elapsed_time(evs[-1])
+
+
+def l2_bytes(dev):
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except (AttributeError, RuntimeError):
+        return 126 << 20
+
+
+def capture(fn, stream):
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
 def run_ours(args, w):
     from decode_sparse_attention_gb300 import questsparse as qs
     ws_, rank, local = dist_env()
@@ -286,72 +324,95 @@ def run_ours(args, w):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     qs.lib()
-    x, mode, sel, out, params, meta_ms = setup(w, args.seed + rank, dev, args.fused_select)
+    stream = torch.cuda.Stream(dev)
     flush = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     sink = torch.zeros((), dtype=torch.int64, device=dev)
-    stream = torch.cuda.Stream(dev)
 
-    # eager warm-up, then capture the step in a graph
+    # input set 0, its step bytes, then as many more sets (same lengths, other
+    # seeds) as it takes for the rotation to exceed 3x the L2
+    sets = [setup(w, args.seed + rank, dev, args.fused_select)]
+    x0, mode, sel0, out0, params0, meta_ms = sets[0]
     with torch.cuda.stream(stream):
         for _ in range(3):
-            qs.sparse_decode_step(params, dev)
+            qs.sparse_decode_step(params0, dev)
     torch.cuda.synchronize()
     assert qs.read_status(dev) == 0
-    g_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step, stream=stream):
-        qs.sparse_decode_step(params, dev)
-    # the selector alone (diagnostic) and the dominant kernel alone (same
-    # selection, same launch configuration)
-    sel2 = torch.empty_like(sel)
-    g_sel = torch.cuda.CUDAGraph()
-    def run_selector():
-        if mode == 0:
-            qs.quest_block_select_paged_in_out_w(x["q"], x["maxblocks"], x["minblocks"],
-                                                 x["meta_block_tables"], x["seq_lens"], x["t"],
-                                                 sel2)
-        else:
-            qs.probe_select(x["q"], x["k_cache"], x["block_tables"], x["seq_lens"], w.k,
-                            w.n_probe, importance=x.get("importance"),
-                            k_scale=x.get("k_scale"), selected=sel2)
-    with torch.cuda.stream(stream):
-        run_selector()
+    q_es = elem_bytes(x0["q"].dtype)
+    nbytes = step_bytes(w, x0, sel0.cpu().numpy(), q_es)
+    n_sets = max(2, math.ceil(3 * l2_bytes(dev) / max(nbytes["step"], 1)) + 1)
+    rotate = n_sets <= args.max_sets
+    if rotate:
+        seq = x0["seq_lens"].cpu().tolist()
+        for i in range(1, n_sets):
+            sets.append(setup(w, args.seed + rank + 1000 * i, dev, args.fused_select,
+                              seq_lens=seq))
+
+    # graphs: the step, the selector alone and the attention alone per set
+    g_step, g_sel, g_attn = [], [], []
+    keep = []   # buffers the captured graphs write into must outlive them
+    for (x, _, sel, out, params, _) in sets:
+        g_step.append(capture(lambda: qs.sparse_decode_step(params, dev), stream))
+        sel2 = torch.empty_like(sel)
+        def run_selector(x=x, sel2=sel2):
+            if mode == 0:
+                qs.quest_block_select_paged_in_out_w(x["q"], x["maxblocks"], x["minblocks"],
+                                                     x["meta_block_tables"], x["seq_lens"],
+                                                     x["t"], sel2)
+            else:
+                qs.probe_select(x["q"], x["k_cache"], x["block_tables"], x["seq_lens"], w.k,
+                                w.n_probe, importance=x.get("importance"),
+                                k_scale=x.get("k_scale"), selected=sel2)
+        g_sel.append(capture(run_selector, stream))
+        attn_out = torch.empty_like(out)
+        def run_attn(x=x, sel=sel, attn_out=attn_out):
+            qs.sparse_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                                  x["seq_lens"], sel, k_scale=x.get("k_scale"),
+                                  v_scale=x.get("v_scale"), out=attn_out)
+        g_attn.append(capture(run_attn, stream))
+        keep.append((sel2, attn_out))
     torch.cuda.synchronize()
-    with torch.cuda.graph(g_sel, stream=stream):
-        run_selector()
-    attn_out = torch.empty_like(out)
-    g_attn = torch.cuda.CUDAGraph()
-    sel_rows = sel.shape[1]
-    with torch.cuda.graph(g_attn, stream=stream):
-        qs.sparse_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
-                              x["seq_lens"], sel, k_scale=x.get("k_scale"),
-                              v_scale=x.get("v_scale"), out=attn_out)
-    torch.cuda.synchronize()
+    # algorithmic bytes: the mean over the sets (selections differ per set)
+    per_set = [step_bytes(w, s[0], s[2].cpu().numpy(), q_es) for s in sets]
+    nbytes = {k: int(round(sum(d[k] for d in per_set) / len(per_set))) for k in per_set[0]}
 
     sampler = ClockSampler(local)
     t_end = time.time() + args.preroll_s
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            flush_l2(flush, sink)
-            g_step.replay()
+        for i in range(args.warmup):
+            if not rotate:
+                flush_l2(flush, sink)
+            g_step[i % len(g_step)].replay()
         while time.time() < t_end:  # keep the clocks under load for the sampler
-            g_step.replay()
+            for g in g_step:
+                g.replay()
     torch.cuda.synchronize()
     barrier()
-    durs = timed_graph(g_step, flush, sink, args.steps, stream)
+    if rotate:
+        durs, span = timed_rotation(g_step, args.steps, stream)
+        step_us = 1000.0 * span / args.steps
+    else:
+        durs = timed_graph(g_step[0], flush, sink, args.steps, stream)
+        step_us = 1000.0 * sum(durs) / len(durs)
     barrier()
-    attn_durs = timed_graph(g_attn, flush, sink, max(args.steps // 2, 3), stream)
-    sel_durs = timed_graph(g_sel, flush, sink, max(args.steps // 4, 3), stream)
+    n_side = max(args.steps // 2, 3)
+    if rotate:
+        _, attn_span = timed_rotation(g_attn, n_side, stream)
+        _, sel_span = timed_rotation(g_sel, n_side, stream)
+        attn_us = 1000.0 * attn_span / n_side
+        sel_us = 1000.0 * sel_span / n_side
+    else:
+        attn_us = 1000.0 * statistics.mean(timed_graph(g_attn[0], flush, sink, n_side, stream))
+        sel_us = 1000.0 * statistics.median(timed_graph(g_sel[0], flush, sink, n_side, stream))
+    # the same step, one at a time after an L2 flush (each bracketed by its
+    # own events: includes the graph launch latency a lone step pays)
+    flushed = timed_graph(g_step[0], flush, sink, max(args.steps // 4, 3), stream)
     clocks = sampler.stop()
     assert qs.read_status(dev) == 0
 
-    step_us = 1000.0 * sum(durs) / len(durs)
-    attn_us = 1000.0 * sum(attn_durs) / len(attn_durs)
     step_us_max = max_over_ranks(step_us, dev)
-    sel_np = sel.cpu().numpy()
-    q_es = elem_bytes(x["q"].dtype)
-    nbytes = step_bytes(w, x, sel_np, q_es)
 
     # end to end through the C ABI from pinned host buffers
+    x, _, _, out, params, _ = sets[0]
     host = {k: x[k].cpu().pin_memory() for k in ("q", "seq_lens", "block_tables",
                                                  "meta_block_tables")}
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -374,6 +435,7 @@ def run_ours(args, w):
 
     peak, peak_kind = hbm_peak()
     achieved = nbytes["attention"] / (attn_us * 1e-6) / 1e9
+    kernels = qs.step_kernels(params0)
     res = {
         "metric": METRIC,
         "value": round(step_us_max, 3),
@@ -386,23 +448,29 @@ def run_ours(args, w):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16",
-                  torch.int8: "i8"}[x["k_cache"].dtype],
+                  torch.int8: "i8"}[x0["k_cache"].dtype],
         "data": "synthetic",
         "config": {
             "workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "block_size": w.BS,
             "seq_len": w.seq_len if w.seq_len else "ragged", "k": w.k,
-            "tokens_since_metadata_update": x["t"], "selector": w.mode,
+            "tokens_since_metadata_update": x0["t"], "selector": w.mode,
             "parallelism": "replicas" if ws_ > 1 else "single GPU",
-            "l2": "256 MiB written then read back between timed steps",
-            "step": "qs_sparse_decode_step replayed as a CUDA graph",
+            "l2": ("inputs larger than L2: %d input sets (same lengths, other seeds) replayed in "
+                   "rotation, %.0f MB of step traffic per rotation vs %d MB of L2"
+                   % (len(sets), len(sets) * nbytes["step"] / 1e6, l2_bytes(dev) >> 20))
+                  if rotate else "256 MiB written then read back between timed steps",
+            "step": "qs_sparse_decode_step captured as one CUDA graph per input set; "
+                    + ("graphs replayed back to back, value = span / steps" if rotate
+                       else "value = mean of per-step event pairs"),
             "fused_select": args.fused_select,
-            "kernels_per_step": qs.step_kernels(params),
+            "kernels_per_step": kernels,
         },
         "step_gbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9, 1),
         "step_frac_of_peak": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / peak, 4),
         "step_frac_of_8tbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / 8000.0, 4),
         "algorithmic_bytes": nbytes,
         "step_us_p10_p50_p90": [round(1000 * float(np.percentile(durs, p)), 3) for p in (10, 50, 90)],
+        "step_us_flushed_single": round(1000.0 * statistics.median(flushed), 3),
         "roofline": {
             "kernel": "sparse_attn_kernel",
             "bound": "hbm",
@@ -415,21 +483,22 @@ def run_ours(args, w):
             "launch_us": round(attn_us, 3),
             "bytes_per_launch": nbytes["attention"],
         },
-        "selector_alone_us": round(1000.0 * statistics.median(sel_durs), 3),
+        "selector_alone_us": round(sel_us, 3),
         "metadata_prefill_us": None if meta_ms is None else round(meta_ms * 1000, 2),
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks,
-        "gpu_launches": qs.step_kernels(params) * args.steps,
+        "gpu_launches": kernels * args.steps,
     }
     if meta_ms is not None:
-        L = x["meta_seq_lens"].cpu().numpy()
-        kbytes = int(sum(int(l) for l in L)) * w.N * w.D * elem_bytes(x["k_cache"].dtype)
-        mrows = sum(((int(l) + w.BS - 1) // w.BS + w.BS - 1) // w.BS * w.BS for l in x["seq_lens"].cpu().numpy())
-        mbytes = mrows * w.N * w.D * elem_bytes(x["k_cache"].dtype) * 2
+        L = x0["meta_seq_lens"].cpu().numpy()
+        kbytes = int(sum(int(l) for l in L)) * w.N * w.D * elem_bytes(x0["k_cache"].dtype)
+        mrows = sum(((int(l) + w.BS - 1) // w.BS + w.BS - 1) // w.BS * w.BS
+                    for l in x0["seq_lens"].cpu().numpy())
+        mbytes = mrows * w.N * w.D * elem_bytes(x0["k_cache"].dtype) * 2
         res["metadata_prefill_gbs"] = round((kbytes + mbytes) / (meta_ms * 1e-3) / 1e9, 1)
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(w, x0, args.cpu_seconds)
     if ws_ > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -565,6 +634,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-sets", type=int, default=24,
+                    help="most input sets to rotate through; workloads needing more (tiny "
+                         "steps) are timed with an L2 flush between steps instead")
     ap.add_argument("--fused-select", type=int, default=-1, choices=[-1, 0, 1],
                     help="Quest step: -1 library's choice, 0 selector + attention kernels, "
                          "1 the fused one-kernel step")

@@ -265,7 +265,7 @@ QS_DEVINL void quest_select_units(const AttnArgs& a, long long u_first, int n_un
         float acc = 0.f;
 #pragma unroll
         for (int g = 0; g < G; ++g) acc += qf[(us * G + g) * D + d];
-        qg_s[e] = acc / static_cast<float>(G);
+        qg_s[e] = group_mean(acc, G);
     }
     // rows of the units, concatenated
     if (tid == 0) {
@@ -326,7 +326,9 @@ QS_DEVINL void quest_select_units(const AttnArgs& a, long long u_first, int n_un
                 const float4 v = *reinterpret_cast<const float4*>(qs + e);
                 qreg[e] = v.x; qreg[e + 1] = v.y; qreg[e + 2] = v.z; qreg[e + 3] = v.w;
             }
-            const float sc = row_score_reduce<kLPR>(RowChunk<KT>::dot(qreg, vmx[r], vmn[r]));
+            RowChunk<KT> rc;
+            rc.prepare(qreg);
+            const float sc = row_score_reduce<kLPR>(rc.dot(vmx[r], vmn[r]));
             if (cl == 0 && row < R) keys[row] = float_key(live[r] ? sc : __int_as_float(0xff800000));
         }
     }
@@ -732,7 +734,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
 
         // ---- end of a unit within this CTA: merge warps, write output/partial
         if (ti.flags & kLast) {
-            const long long t = t0 + i;
             const int u = static_cast<int>(u_first + ti.unit);
             float* accw = reinterpret_cast<float*>(cur);     // this warp's consumed stage slot
             if (rep && tq == 0) {

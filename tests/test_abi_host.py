@@ -53,7 +53,7 @@ def test_status_strings_and_version(built_lib):
 def test_workspace_size_without_gpu(built_lib):
     from decode_sparse_attention_gb300 import questsparse as qs
     n = qs.workspace_size(qs.OP_BLOCK_SELECT, 20, 32, 8, 128, 128, 8, 128, 8)
-    assert n >= 20 * 8 * 128 * 4 + 20 * 8 * 4
+    assert n >= 20 * 8 * 128 * 4                      # one fp32 score per block and KV head
     a = qs.workspace_size(qs.OP_SPARSE_ATTN, 20, 32, 8, 128, 128, 8, 128, 8)
     assert a >= 160 * 4 + 160 * 4 * 130 * 4
     s = qs.workspace_size(qs.OP_STEP_QUEST, 20, 32, 8, 128, 128, 8, 128, 8)

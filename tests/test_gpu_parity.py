@@ -52,6 +52,11 @@ QUEST_CASES = {
     "g1_fp32q": W["bf16_paged"].replace(B=2, H=8, N=8, seq_len=5000, MMBPR=None, k=5,
                                         q_dtype="f32", t=3),
     "g2_bs16": W["tiny_fp32"].replace(B=3, seq_len=777, k=7, kv_dtype="bf16", q_dtype="bf16"),
+    # units of 1..3 scoring chunks: the persistent chunk-queue selector
+    "ragged_multi_chunk": W["ragged"].replace(B=6, ragged=(100, 40000, 1), MMBPR=None, k=8),
+    "ragged_multi_chunk_window": W["ragged"].replace(B=5, ragged=(5000, 40000, 1), MMBPR=None,
+                                                     k=10, t=50),
+    "fp32_d64_multi_chunk": W["tiny_fp32"].replace(B=3, seq_len=9000, k=6),
 }
 
 
@@ -144,6 +149,35 @@ def test_quest_needle_selected(seed):
     _, j, _ = x["needle"]
     for n in range(w.N):
         assert j in gsel[0, n].tolist()
+
+
+def test_quest_select_queue_empty_and_long_requests():
+    """Chunk-queue selector: an empty request and a one-block request among
+    multi-chunk ones; every unit is emitted once, padded with -1."""
+    w = W["ragged"].replace(B=4, seq_len=None, ragged=(1, 2, 1), MMBPR=None, k=6)
+    x, g = make(w, seed=3, seq_lens=[0, 30000, 77, 41000])
+    gsel, gsc = run_quest(w, x, g)
+    assert np.all(gsel[0] == -1) and np.all(gsel[2, :, 1:] == -1) and np.all(gsel[2, :, 0] == 0)
+    _, exact = compare_quest(w, x, gsel, gsc, "queue-empty-long")
+    assert exact >= 0.9 * w.B * w.N
+
+
+def test_quest_select_queue_bad_length_is_reported():
+    w = W["ragged"].replace(B=3, seq_len=None, ragged=(1, 2, 1), MMBPR=None, k=6)
+    x, g = make(w, seed=1, seq_lens=[20000, 30000, 500])
+    sl = g["seq_lens"].clone()
+    sl[1] = 10 ** 8                      # more blocks than the metadata table holds
+    qs.quest_prefill_metadata(g["k_cache"], g["meta_seq_lens"], g["block_tables"],
+                              g["meta_block_tables"], g["maxblocks"], g["minblocks"])
+    sel = torch.full((w.B, w.N, w.k), -5, dtype=torch.int32, device=DEV)
+    for _ in range(2):                   # the queue counters rearm after an error too
+        qs.quest_block_select_paged_in_out_w(g["q"], g["maxblocks"], g["minblocks"],
+                                             g["meta_block_tables"], sl, x["t"], sel)
+        torch.cuda.synchronize()
+        assert qs.read_status(DEV) == 3  # QS_DEV_ESEQ_LEN
+        assert torch.all(sel[1] == -1)
+    gsel, gsc = run_quest(w, x, g)       # and a clean call still matches the oracle
+    compare_quest(w, x, gsel, gsc, "queue-after-error")
 
 
 def test_quest_select_deterministic():
