@@ -199,7 +199,7 @@ def hbm_peak():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("qs_attention.cu", "qs_common.cuh"):
+    for f in ("qs_attention.cu", "qs_attention_kernel.cuh", "qs_common.cuh"):
         with open(os.path.join(ROOT, "decode_sparse_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     __shared__ float s_sq[G];
     __shared__ TopkFastScratch s_fast;
     __shared__ TopkScratch<kThreads> s_topk;
+    __shared__ unsigned long long s_best;   // recency: lowest (probe key, index) pick
     __shared__ int s_last;
 
     pdl_launch_dependents();
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         if (want > 0 && !(flags[nb - 1] & (kFixed | kPick))) {
             // the last block replaces the probe pick with the lowest probe
             // score (ties: the larger index); importance picks stay
-            if (threadIdx.x == 0) s_topk.best = ~0ull;
+            if (threadIdx.x == 0) s_best = ~0ull;
             __syncthreads();
             unsigned long long mine = ~0ull;
             for (int j = threadIdx.x; j < nb; j += kThreads)
@@ -342,10 +343,10 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
                         (static_cast<unsigned long long>(keys[j]) << 32) | (0xffffffffu - static_cast<uint32_t>(j));
                     mine = c < mine ? c : mine;
                 }
-            atomicMin(&s_topk.best, mine);
+            atomicMin(&s_best, mine);
             __syncthreads();
             if (threadIdx.x == 0) {
-                const int victim = static_cast<int>(0xffffffffu - static_cast<uint32_t>(s_topk.best & 0xffffffffu));
+                const int victim = static_cast<int>(0xffffffffu - static_cast<uint32_t>(s_best & 0xffffffffu));
                 flags[victim] &= static_cast<uint8_t>(~kPick);
                 flags[nb - 1] |= kPick;
             }

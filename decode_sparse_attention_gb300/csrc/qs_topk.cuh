@@ -1,15 +1,12 @@
-// CTA-wide deterministic top-k over keys held in shared memory.
+// Deterministic top-k over keys held in shared memory, block-wide and
+// one-warp forms.
 //
 // Order: larger key first, equal keys by lower index first, no randomness
 // (Kestrel-LLM 10-2 section 1: ties are broken by the block index;
 // CANN Quest page step 2.3: top-k over all blocks of the request).
 //
-// Method: an MSB-first radix select over the 32-bit keys (4 passes of 8-bit
-// digits, histograms with warp-aggregated shared-memory atomics) finds the
-// k-th largest key T and how many keys equal to T are taken; the picks are
-// every candidate key > T plus the first keys == T in index order (a
-// CTA-wide prefix count).  The result is a set, returned as flags, so the
-// cost is independent of k.
+// The result is a set, returned as flags (kPick), so the cost does not grow
+// with k; callers emit the picked indices in ascending order.
 //
 // Every routine runs on all threads of the block (blockDim.x, a multiple of
 // 32, at most NT: the template argument only sizes the scratch).
@@ -21,13 +18,9 @@ namespace qs {
 
 enum : uint8_t { kCand = 1, kPick = 2, kFixed = 4 };
 
+// Scratch of a block-wide exclusive scan (one partial per warp).
 template <int NT> struct TopkScratch {
-    uint32_t hist[2][256];   // double-buffered: one pass fills, the next is cleared
     int warp_sums[NT / 32 + 1];
-    uint32_t prefix;
-    int remaining;
-    int count;
-    unsigned long long best;
 };
 
 // Exclusive prefix sum of v over the CTA in thread order; total in *total.
@@ -59,98 +52,6 @@ QS_DEVINL int block_exclusive_scan(int v, TopkScratch<NT>& s, int* total) {
     return before + x - v;
 }
 
-// Sets kPick on the top `want` entries among those flagged kCand.
-// Requires 0 <= want <= number of candidates.
-template <int NT>
-QS_DEVINL void topk_flags(const uint32_t* keys, uint8_t* flags, int n, int want,
-                          TopkScratch<NT>& s) {
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int nt = static_cast<int>(blockDim.x);
-    if (want <= 0) return;
-    for (int i = tid; i < 256; i += nt) s.hist[0][i] = 0;
-    __syncthreads();
-    uint32_t prefix = 0, mask = 0;
-    int remaining = want;
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        uint32_t* hist = s.hist[pass & 1];
-        for (int base = 0; base < n; base += nt) {
-            const int j = base + tid;
-            bool ok = false;
-            uint32_t digit = 0x100u + lane;
-            if (j < n && (flags[j] & kCand)) {
-                const uint32_t key = keys[j];
-                if ((key & mask) == prefix) {
-                    ok = true;
-                    digit = (key >> shift) & 0xffu;
-                }
-            }
-            const unsigned peers = __match_any_sync(0xffffffffu, digit);
-            if (ok && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
-        }
-        // the other buffer is idle during this pass: clear it for the next
-        for (int i = tid; i < 256; i += nt) s.hist[(pass + 1) & 1][i] = 0;
-        __syncthreads();
-        if (tid < 32) {
-            // lane l owns digits 255-8l ... 248-8l (descending)
-            uint32_t c[8];
-            uint32_t sum = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                c[i] = hist[255 - 8 * lane - i];
-                sum += c[i];
-            }
-            uint32_t incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t excl = incl - sum;
-            // the lane whose range first reaches `remaining`
-            const bool hit = excl < static_cast<uint32_t>(remaining) &&
-                             incl >= static_cast<uint32_t>(remaining);
-            if (hit) {
-                uint32_t above = excl;
-                int d = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (above + c[i] >= static_cast<uint32_t>(remaining)) {
-                        d = 255 - 8 * lane - i;
-                        break;
-                    }
-                    above += c[i];
-                }
-                s.prefix = prefix | (static_cast<uint32_t>(d) << shift);
-                s.remaining = remaining - static_cast<int>(above);
-            }
-        }
-        __syncthreads();
-        prefix = s.prefix;
-        remaining = s.remaining;
-        mask |= 0xffu << shift;
-    }
-    // prefix = T (the want-th largest key); take every key > T and the first
-    // `remaining` keys == T in index order.
-    const int per = (n + nt - 1) / nt;
-    const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
-    int eq = 0;
-    for (int j = j0; j < j1; ++j) eq += (flags[j] & kCand) && keys[j] == prefix;
-    int tot;
-    int before = block_exclusive_scan<NT>(eq, s, &tot);
-    for (int j = j0; j < j1; ++j) {
-        if (!(flags[j] & kCand)) continue;
-        const uint32_t key = keys[j];
-        if (key > prefix) {
-            flags[j] |= kPick;
-        } else if (key == prefix) {
-            if (before < remaining) flags[j] |= kPick;
-            ++before;
-        }
-    }
-    __syncthreads();
-}
-
 QS_DEVINL unsigned lanemask_lt() {
     unsigned m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -158,43 +59,49 @@ QS_DEVINL unsigned lanemask_lt() {
 }
 
 // ---------------------------------------------------------------------------
-// Histogram top-k: one pass of a 256-bin histogram over the bits right
-// below the common prefix of the candidate keys finds the bin that holds the
-// want-th key; bins above it are taken whole and the few keys inside the
-// boundary bin are ranked exactly (key desc, index asc) by one warp.  Five
-// block barriers in the common case; falls back to the 4-pass radix
-// selection when the boundary bin holds more than kListMax keys.
+// Histogram top-k: MSB-first radix selection with 8-bit digits below the
+// candidates' common key prefix.  Each level builds a 256-bin histogram of
+// the digit over the keys still in play (shared-memory atomics, one copy of
+// the bins per warp of a group of eight, summed by the scan), one warp
+// finds the digit that holds the want-th key, keys with a larger digit are
+// taken, and the boundary digit is refined with the next 8 bits until at
+// most kListMax keys remain in it; those are ranked exactly (key descending,
+// lower index first) by four threads per key.  If all 32 bits get fixed, the
+// remaining keys are equal and the lowest indices are taken.  Four block
+// barriers per level; usually one or two levels.
 // ---------------------------------------------------------------------------
 
 constexpr int kHistBins = 256;
+constexpr int kHistCopies = 8;   // warp w counts into copy w % 8: no inter-warp contention
 constexpr int kListMax = 64;
 
 struct TopkFastScratch {
-    __align__(16) uint32_t hist[kHistBins];
+    __align__(16) uint32_t hist[kHistCopies][kHistBins];
     uint32_t list_key[kListMax];
     int list_idx[kListMax];
     uint32_t wmax[32], wmin[32];
     int wcnt[32];
-    int nlist, dstar, remaining, overflow;
+    int nlist, dstar, remaining, inbin;
 };
 
 // Clears the histogram; call before topk_fast with a barrier in between
 // (the scoring phase of the callers provides it).
 template <int NT>
 QS_DEVINL void topk_fast_clear(TopkFastScratch& s) {
-    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) s.hist[i] = 0;
+    for (int i = threadIdx.x; i < kHistCopies * kHistBins; i += blockDim.x) (&s.hist[0][0])[i] = 0;
     if (threadIdx.x == 0) s.nlist = 0;
 }
 
 // Sets kPick on the top `want` entries among those flagged kCand (keys and
-// flags in shared memory).  Requires the histogram cleared beforehand.
+// flags in shared memory).  Requires the histogram cleared beforehand and at
+// least 4 * kListMax threads.
 template <int NT>
 QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
                          TopkFastScratch& s, TopkScratch<NT>& rs) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NT_ = static_cast<int>(blockDim.x), NW = NT_ >> 5;   // NT_ <= NT
     if (want <= 0) return;
-    // 0. candidate count and key range
+    // candidate count and key range
     uint32_t lmax = 0, lmin = 0xffffffffu;
     int lc = 0;
     for (int j = tid; j < n; j += NT_)
@@ -215,10 +122,13 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
     __syncthreads();
     uint32_t kmax = 0, kmin = 0xffffffffu;
     int ncand = 0;
-    for (int w = 0; w < NW; ++w) {
-        kmax = max(kmax, s.wmax[w]);
-        kmin = min(kmin, s.wmin[w]);
-        ncand += s.wcnt[w];
+    {
+        const uint32_t a = lane < NW ? s.wmax[lane] : 0u;
+        const uint32_t b = lane < NW ? s.wmin[lane] : 0xffffffffu;
+        const int c = lane < NW ? s.wcnt[lane] : 0;
+        kmax = __reduce_max_sync(0xffffffffu, a);
+        kmin = __reduce_min_sync(0xffffffffu, b);
+        ncand = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
     }
     if (want >= ncand) {          // everything goes
         for (int j = tid; j < n; j += NT_)
@@ -226,87 +136,126 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
         __syncthreads();
         return;
     }
+    // keys in play: candidates whose bits under pmask equal prefix
     const uint32_t diff = kmax ^ kmin;
-    const int top = diff ? 31 - __clz(diff) : 0;
-    const int lo = top >= 7 ? top - 7 : 0;
-    const int nbins = 1 << (top - lo + 1);
-    const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
-    // 1. histogram of the digit below the common prefix
-    for (int j = tid; j < n; j += NT_)
-        if (flags[j] & kCand) atomicAdd(&s.hist[(keys[j] >> lo) & dmask], 1u);
-    __syncthreads();
-    // 2. boundary bin: one warp scans the 256 bins from the top, 8 per lane
-    //    (two 16-byte loads each)
-    if (warp == 0) {
-        const int d_hi = kHistBins - 1 - 8 * lane;          // lane's bins d_hi .. d_hi-7
-        const uint4 h0 = *reinterpret_cast<const uint4*>(&s.hist[d_hi - 7]);
-        const uint4 h1 = *reinterpret_cast<const uint4*>(&s.hist[d_hi - 3]);
-        const int cnt[8] = {static_cast<int>(h1.w), static_cast<int>(h1.z), static_cast<int>(h1.y),
-                            static_cast<int>(h1.x), static_cast<int>(h0.w), static_cast<int>(h0.z),
-                            static_cast<int>(h0.y), static_cast<int>(h0.x)};   // descending bins
-        int c = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) c += cnt[i];
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const int excl = incl - c;
-        if (excl < want && incl >= want) {
-            int above = excl;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (above + cnt[i] >= want) {
-                    s.dstar = d_hi - i;
-                    s.remaining = want - above;
-                    break;
-                }
-                above += cnt[i];
-            }
-        }
-    }
-    __syncthreads();
-    const uint32_t dstar = static_cast<uint32_t>(s.dstar);
-    // 3. above the boundary: taken; inside: listed
-    for (int j = tid; j < n; j += NT_)
-        if (flags[j] & kCand) {
-            const uint32_t d = (keys[j] >> lo) & dmask;
-            if (d > dstar) {
-                flags[j] |= kPick;
-            } else if (d == dstar) {
-                const int pos = atomicAdd(&s.nlist, 1);
-                if (pos < kListMax) {
-                    s.list_key[pos] = keys[j];
-                    s.list_idx[pos] = j;
-                }
-            }
-        }
-    __syncthreads();
-    const int nlist = s.nlist;
-    if (nlist <= kListMax) {
-        // 4. exact ranks inside the boundary bin
+    int hi = diff ? 31 - __clz(diff) : -1;              // highest bit not yet fixed
+    uint32_t pmask = hi < 0 ? 0xffffffffu : (hi >= 31 ? 0u : ~((2u << hi) - 1u));
+    uint32_t prefix = kmax & pmask;
+    int remaining = want;
+    while (hi >= 0) {
+        const int lo = hi >= 7 ? hi - 7 : 0;
+        const uint32_t dmask = (2u << (hi - lo)) - 1u;
+        // histogram of the digit over the keys in play (the bins are clear);
+        // each warp counts into its own copy (keys of similar magnitude
+        // crowd a few bins, and same-address atomics serialise; measured on
+        // GB300, warp-aggregating them first with match_any was slower)
+        for (int j = tid; j < n; j += NT_)
+            if ((flags[j] & kCand) && (keys[j] & pmask) == prefix)
+                atomicAdd(&s.hist[warp % kHistCopies][(keys[j] >> lo) & dmask], 1u);
+        __syncthreads();
+        // boundary digit: warp 0 scans the 256 bins from the top, 8 per lane
         if (warp == 0) {
-            const int remaining = s.remaining;
-            for (int e = lane; e < nlist; e += 32) {
-                const uint32_t ke = s.list_key[e];
-                const int ie = s.list_idx[e];
-                int rank = 0;
-                for (int f = 0; f < nlist; ++f) {
-                    const uint32_t kf = s.list_key[f];
-                    rank += kf > ke || (kf == ke && s.list_idx[f] < ie);
+            const int d_hi = kHistBins - 1 - 8 * lane;      // lane's bins d_hi .. d_hi-7
+            uint4 h0 = make_uint4(0, 0, 0, 0), h1 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int cp = 0; cp < kHistCopies; ++cp) {
+                const uint4 a0 = *reinterpret_cast<const uint4*>(&s.hist[cp][d_hi - 7]);
+                const uint4 a1 = *reinterpret_cast<const uint4*>(&s.hist[cp][d_hi - 3]);
+                h0.x += a0.x; h0.y += a0.y; h0.z += a0.z; h0.w += a0.w;
+                h1.x += a1.x; h1.y += a1.y; h1.z += a1.z; h1.w += a1.w;
+            }
+            const int cnt[8] = {static_cast<int>(h1.w), static_cast<int>(h1.z), static_cast<int>(h1.y),
+                                static_cast<int>(h1.x), static_cast<int>(h0.w), static_cast<int>(h0.z),
+                                static_cast<int>(h0.y), static_cast<int>(h0.x)};   // descending bins
+            int c = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c += cnt[i];
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int excl = incl - c;
+            if (excl < remaining && incl >= remaining) {
+                int above = excl;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (above + cnt[i] >= remaining) {
+                        s.dstar = d_hi - i;
+                        s.remaining = remaining - above;
+                        s.inbin = cnt[i];
+                        break;
+                    }
+                    above += cnt[i];
                 }
-                if (rank < remaining) flags[ie] |= kPick;
             }
         }
         __syncthreads();
-        return;
+        const uint32_t dstar = static_cast<uint32_t>(s.dstar);
+        remaining = s.remaining;
+        const int inbin = s.inbin;
+        // digits above the boundary are taken; the boundary digit is listed
+        // when it is small; the bins are cleared for a next level
+        const bool last_level = inbin == remaining || inbin <= kListMax;
+        for (int j = tid; j < n; j += NT_)
+            if ((flags[j] & kCand) && (keys[j] & pmask) == prefix) {
+                const uint32_t d = (keys[j] >> lo) & dmask;
+                if (d > dstar) {
+                    flags[j] |= kPick;
+                } else if (d == dstar) {
+                    if (inbin == remaining) {
+                        flags[j] |= kPick;
+                    } else if (inbin <= kListMax) {
+                        const int pos = atomicAdd(&s.nlist, 1);
+                        s.list_key[pos] = keys[j];
+                        s.list_idx[pos] = j;
+                    }
+                }
+            }
+        if (!last_level)
+            for (int i = tid; i < kHistCopies * kHistBins; i += NT_) (&s.hist[0][0])[i] = 0;
+        __syncthreads();
+        if (last_level) {
+            if (inbin != remaining) {
+                // exact ranks inside the boundary digit, four threads per key
+                const int nlist = s.nlist;
+                const int e = tid >> 2, part = tid & 3;
+                int rank = 0;
+                uint32_t ke = 0;
+                int ie = 0;
+                if (e < nlist) {
+                    ke = s.list_key[e];
+                    ie = s.list_idx[e];
+                    for (int f = part; f < nlist; f += 4) {
+                        const uint32_t kf = s.list_key[f];
+                        rank += kf > ke || (kf == ke && s.list_idx[f] < ie);
+                    }
+                }
+                rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+                rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+                if (part == 0 && e < nlist && rank < remaining) flags[ie] |= kPick;
+                __syncthreads();
+            }
+            return;
+        }
+        prefix |= dstar << lo;
+        pmask |= dmask << lo;
+        hi = lo - 1;
     }
-    // a crowded boundary bin (many equal keys): exact radix selection
-    for (int j = tid; j < n; j += NT_) flags[j] &= static_cast<uint8_t>(~kPick);
+    // every bit fixed: the keys in play are equal; take the lowest indices
+    const int per = (n + NT_ - 1) / NT_;
+    const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
+    int eq = 0;
+    for (int j = j0; j < j1; ++j) eq += (flags[j] & kCand) && keys[j] == prefix;
+    int tot;
+    int before = block_exclusive_scan<NT>(eq, rs, &tot);
+    for (int j = j0; j < j1; ++j)
+        if ((flags[j] & kCand) && keys[j] == prefix) {
+            if (before < remaining) flags[j] |= kPick;
+            ++before;
+        }
     __syncthreads();
-    topk_flags<NT>(keys, flags, n, want, rs);
 }
 
 // One warp writes the indices j with (flags[j] & bits) in ascending order
