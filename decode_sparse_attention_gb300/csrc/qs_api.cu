@@ -1,8 +1,5 @@
-// Host side of the C ABI: device queries, tensor-map encoding, status
-// strings, workspace sizing and the fused decode step.
-#include <cudaTypedefs.h>
-
-#include <cstring>
+// Host side of the C ABI: device queries, status strings, workspace sizing
+// and the decode step.
 #include <map>
 #include <mutex>
 #include <utility>
@@ -14,9 +11,6 @@ namespace qs {
 namespace {
 constexpr int kMaxDevices = 64;
 int g_sms[kMaxDevices];
-std::mutex g_mu;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-bool g_encode_tried = false;
 }  // namespace
 
 int num_sms() {
@@ -46,39 +40,6 @@ bool ensure_smem(const void* func, size_t bytes) {
         return false;
     done[key] = want;
     return true;
-}
-
-bool encode_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
-               uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows) {
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_encode_tried) {
-            g_encode_tried = true;
-            void* fn = nullptr;
-            cudaDriverEntryPointQueryResult qr;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                 cudaEnableDefault, &qr) == cudaSuccess &&
-                qr == cudaDriverEntryPointSuccess)
-                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-    }
-    if (!g_encode) return false;
-    CUtensorMapDataType dt;
-    switch (elem_bytes) {
-        case 1: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
-        case 2: dt = CU_TENSOR_MAP_DATA_TYPE_UINT16; break;
-        case 4: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
-        default: return false;
-    }
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {row_stride_bytes};
-    const cuuint32_t box[2] = {box_cols, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    std::memset(map, 0, sizeof(*map));
-    return g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace qs

@@ -22,10 +22,6 @@ QS_DEVINL void set_status(int32_t* st, int code) {
     if (st) atomicCAS(st, 0, code);
 }
 
-// Upper bound of spins on an mbarrier before a wait gives up (several seconds
-// at the try_wait suspend granularity).
-constexpr uint32_t kSpinLimit = 1u << 26;
-
 // ---------------------------------------------------------------------------
 // element types
 // ---------------------------------------------------------------------------
@@ -146,58 +142,11 @@ QS_DEVINL uint32_t float_key(float f) {
 }
 
 // ---------------------------------------------------------------------------
-// mbarrier + TMA (inline PTX)
+// shared-memory addresses and launch controls (inline PTX)
 // ---------------------------------------------------------------------------
 
 QS_DEVINL uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-QS_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
-QS_DEVINL void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-QS_DEVINL void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-QS_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
-                     smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-QS_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2; "
-        "selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait: returns false if the barrier did not complete in time.
-QS_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-// 2-D tiled TMA load of box {x: inner elements, y: rows} into shared memory,
-// completing on `bar` with a transaction count of the box's bytes.
-QS_DEVINL void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
-QS_DEVINL void prefetch_tensormap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // Programmatic dependent launch controls.
@@ -205,12 +154,6 @@ QS_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 QS_DEVINL void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
-
-QS_DEVINL void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-QS_DEVINL int lane_id() { return threadIdx.x & 31; }
 
 }  // namespace qs
 
@@ -220,12 +163,6 @@ QS_DEVINL int lane_id() { return threadIdx.x & 31; }
 namespace qs {
 int num_sms();                      // of the current device (cached per device)
 cudaError_t last_launch_error();
-// Encodes a 2-D tiled tensor map over a row-major [rows, cols] array of
-// `elem_bytes` elements with row stride `row_stride_bytes`, box {box_cols,
-// box_rows}.  Returns false if the driver entry point is unavailable or the
-// encode fails.
-bool encode_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
-               uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows);
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device; the attribute is set once per (kernel, device) so that
