@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
     static_assert(EPL % 2 == 0, "P.V uses fp32 pairs");
 
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int s_last;
+    __shared__ int s_lastv[2];   // this CTA arrived last for s_split[i]
     __shared__ int s_split[2];   // units of this CTA shared with other CTAs
     __shared__ int s_nsplit;
     TileInfo* info = reinterpret_cast<TileInfo*>(smem);
@@ -800,49 +800,54 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
     cp_async_wait(0);
 
     // ---- units this CTA shares with others: the last CTA to arrive merges
-    // the (max, sum, acc) partials of all of them
+    // the (max, sum, acc) partials of all of them.  One fence for all of this
+    // CTA's partials, then every shared unit's arrival in the same round trip.
     __syncthreads();
     const int nsplit = s_nsplit;
     if (nsplit > 0) {
         __threadfence();
         __syncthreads();
+        if (tid < nsplit) {
+            const int u = s_split[tid];
+            const long long ut0 = static_cast<long long>(u) * tpu, ut1 = ut0 + tpu;
+            const int c_first = static_cast<int>(ut0 / a.tpc);
+            const int c_last = static_cast<int>((ut1 - 1) / a.tpc);
+            const uint32_t prev = atomicAdd(&a.counters[u], 1u);
+            const bool last = prev == static_cast<uint32_t>(c_last - c_first);
+            if (last) a.counters[u] = 0;  // rearm for the next call
+            s_lastv[tid] = last;
+        }
+        __syncthreads();
         for (int k2 = 0; k2 < nsplit; ++k2) {
+            if (!s_lastv[k2]) continue;   // uniform: shared memory
+            __threadfence();
             const int u = s_split[k2];
             const long long ut0 = static_cast<long long>(u) * tpu, ut1 = ut0 + tpu;
             const int c_first = static_cast<int>(ut0 / a.tpc);
             const int c_last = static_cast<int>((ut1 - 1) / a.tpc);
-            if (tid == 0) {
-                const uint32_t prev = atomicAdd(&a.counters[u], 1u);
-                const bool last = prev == static_cast<uint32_t>(c_last - c_first);
-                if (last) a.counters[u] = 0;  // rearm for the next call
-                s_last = last;
-            }
-            __syncthreads();
-            if (s_last) {
-                __threadfence();
-                const int b = u / a.sel_heads, s = u % a.sel_heads;
-                const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
-                for (int idx = tid; idx < G * D; idx += nthreads) {
-                    const int h = idx / D, d = idx % D;
-                    float M = -INFINITY;
-                    for (int cc = c_first; cc <= c_last; ++cc)
-                        M = fmaxf(M, ldcg_f32(a.partial + static_cast<size_t>(cc + u) * G * (D + 2) + h));
-                    float Ls = 0.f, A = 0.f;
-                    if (M != -INFINITY) {
-                        for (int cc = c_first; cc <= c_last; ++cc) {
-                            const float* sl = a.partial + static_cast<size_t>(cc + u) * G * (D + 2);
-                            const float f = exp2_approx(ldcg_f32(sl + h) - M);
-                            Ls += ldcg_f32(sl + G + h) * f;
-                            A += ldcg_f32(sl + 2 * G + h * D + d) * f;
-                        }
+            const int b = u / a.sel_heads, s = u % a.sel_heads;
+            const int h0 = a.sel_heads == a.N ? s * G_per_kv : s;
+            for (int idx = tid; idx < G * D; idx += nthreads) {
+                const int h = idx / D, d = idx % D;
+                float M = -INFINITY;
+#pragma unroll 4
+                for (int cc = c_first; cc <= c_last; ++cc)
+                    M = fmaxf(M, ldcg_f32(a.partial + static_cast<size_t>(cc + u) * G * (D + 2) + h));
+                float Ls = 0.f, A = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll 4
+                    for (int cc = c_first; cc <= c_last; ++cc) {
+                        const float* sl = a.partial + static_cast<size_t>(cc + u) * G * (D + 2);
+                        const float f = exp2_approx(ldcg_f32(sl + h) - M);
+                        Ls += ldcg_f32(sl + G + h) * f;
+                        A += ldcg_f32(sl + 2 * G + h * D + d) * f;
                     }
-                    a.out[(static_cast<size_t>(b) * a.H + h0 + h) * D + d] = Ls > 0.f ? A / Ls : 0.f;
-                    if (d == 0 && a.lse)
-                        a.lse[static_cast<size_t>(b) * a.H + h0 + h] =
-                            Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
                 }
+                a.out[(static_cast<size_t>(b) * a.H + h0 + h) * D + d] = Ls > 0.f ? A / Ls : 0.f;
+                if (d == 0 && a.lse)
+                    a.lse[static_cast<size_t>(b) * a.H + h0 + h] =
+                        Ls > 0.f ? (M + log2f(Ls)) * 0.69314718055994531f : -INFINITY;
             }
-            __syncthreads();
         }
     }
 }

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     uint32_t* dst_pkeys = pkeys;
     if constexpr (MODE == kCluster)
         dst_pkeys = cooperative_groups::this_cluster().map_shared_rank(pkeys, 0);
-    topk_fast_clear<kThreads>(s_fast);
+    topk_fast_clear<kThreads>(s_fast, nb);
 
     // queries of the group (fp32), plus the int8 quantisation for int8 caches
     for (int i = threadIdx.x; i < G * D; i += kThreads) {
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     for (int h = 0; h < G; ++h) {
         const size_t row = static_cast<size_t>(b) * a.H + n * G + h;
         const uint32_t* keys = pkeys + static_cast<size_t>(h) * a.MKBPR;
-        topk_fast_clear<kThreads>(s_fast);
+        topk_fast_clear<kThreads>(s_fast, nb);
         for (int j = threadIdx.x; j < nb; j += kThreads) flags[j] = imp_flags[j] ? kFixed : kCand;
         __syncthreads();
         topk_fast<kThreads>(keys, flags, nb, want, s_fast, s_topk);
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
             }
             __syncthreads();
         }
-        if (warp == 0) warp_emit_flags(flags, kFixed | kPick, nb, a.k, a.selected + row * a.k);
+        block_emit_flags<kThreads>(flags, kFixed | kPick, nb, a.k, a.selected + row * a.k, s_topk);
         __syncthreads();
     }
 }

@@ -20,7 +20,7 @@
 //    A second kernel, a programmatic dependent of the scan, selects one unit
 //    per CTA from those scores.
 // Selection: histogram top-k (key descending, ties to the lower index), then
-// one warp writes the indices in ascending order.
+// the block writes the indices in ascending order.
 #include <algorithm>
 
 #include "qs_internal.cuh"
@@ -170,7 +170,6 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
 QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, const uint32_t* keys_s,
                            uint8_t* flags, int32_t* sel_out, TopkFastScratch& s_fast,
                            TopkScratch<kThreads>& s_topk) {
-    const int warp = threadIdx.x >> 5;
     const int w0 = forced_window_start(L, a.BS, nb, a.t);   // nb: no window
     const int n_forced = forced_count(nb, w0, a.t);
     if (n_forced > a.k) {
@@ -179,13 +178,13 @@ QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, const uint32_t* k
         __syncthreads();
         return;
     }
-    topk_fast_clear<kThreads>(s_fast);
+    topk_fast_clear<kThreads>(s_fast, nb);
     for (int j = threadIdx.x; j < nb; j += kThreads)
         flags[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
     __syncthreads();
     const int want = min(a.k - n_forced, nb - n_forced);
     topk_fast<kThreads>(keys_s, flags, nb, want, s_fast, s_topk);
-    if (warp == 0) warp_emit_flags(flags, kFixed | kPick, nb, a.k, sel_out);
+    block_emit_flags<kThreads>(flags, kFixed | kPick, nb, a.k, sel_out, s_topk);
     __syncthreads();
 }
 
