@@ -13,12 +13,14 @@
 // GB300 design: grid = (block chunks, B*N).  A CTA scores a chunk of blocks
 // for all H/N query heads of one KV head, so each probed K row is read once
 // for the whole group; every lane group has all probe rows of its two blocks
-// in flight at once.  A unit of 2..8 chunks runs as a thread-block cluster
-// whose CTAs write their probe scores into the leader CTA's shared memory
-// (larger units use a global buffer and an arrival counter).  The leader
-// then selects for each query head: histogram top-k passes for the
-// importance picks and the probe fill, a min-reduction for the recency
-// eviction, and one warp writes the indices in ascending order.
+// in flight at once, and while they are, its warps sum the prefill
+// importance of the chunk's blocks (one warp per block, in token order).  A
+// unit of 2..8 chunks runs as a thread-block cluster whose CTAs write their
+// probe scores and importance sums into the leader CTA's shared memory
+// (larger units use global buffers and an arrival counter).  The leader then
+// selects for each query head: histogram top-k passes for the importance
+// picks and the probe fill, a min-reduction for the recency eviction, and the
+// indices written in ascending order.
 #include <cooperative_groups.h>
 
 #include "qs_internal.cuh"
@@ -44,6 +46,7 @@ struct ProbeArgs {
     int B, H, N, BS, k, n_probe;
     int32_t* selected;     // [B, H, k]
     float* probe;          // [B*H, MKBPR]
+    float* isum;           // [B*N, MKBPR] block importance sums (global mode)
     uint32_t* counters;    // [B*N]
     int32_t* dev_status;
 };
@@ -136,8 +139,11 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     uint8_t* flags = reinterpret_cast<uint8_t*>(ikeys + a.MKBPR);
     uint8_t* imp_flags = flags + a.MKBPR;
     uint32_t* dst_pkeys = pkeys;
-    if constexpr (MODE == kCluster)
+    uint32_t* dst_ikeys = ikeys;
+    if constexpr (MODE == kCluster) {
         dst_pkeys = cooperative_groups::this_cluster().map_shared_rank(pkeys, 0);
+        dst_ikeys = cooperative_groups::this_cluster().map_shared_rank(ikeys, 0);
+    }
     topk_fast_clear<kThreads>(s_fast, nb);
 
     // queries of the group (fp32), plus the int8 quantisation for int8 caches
@@ -222,6 +228,27 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
             }
         }
     }
+    // importance of this chunk's blocks while the probe rows are in flight:
+    // one warp per block, coalesced loads, the sum taken in token order (fp32,
+    // sequential, as the importance picks require)
+    if (a.importance) {
+        const float* imp = a.importance + static_cast<size_t>(b) * a.imp_stride;
+        for (int jj = warp; jj < kBlocksPerChunk; jj += kThreads / 32) {
+            const int j = blockIdx.x * kBlocksPerChunk + jj;
+            if (j >= nb) break;   // warp-uniform
+            const int p0 = j * BS, p_end = min(p0 + BS, L);
+            float sacc = 0.f;
+            for (int base = p0; base < p_end; base += 32) {
+                const float v = base + lane < p_end ? imp[base + lane] : 0.f;
+                const int cnt = min(32, p_end - base);
+                for (int t = 0; t < cnt; ++t) sacc = __fadd_rn(sacc, __shfl_sync(0xffffffffu, v, t));
+            }
+            if (lane == 0) {
+                if (MODE != kGlobal) dst_ikeys[j] = float_key(sacc);
+                else a.isum[static_cast<size_t>(u) * a.MKBPR + j] = sacc;
+            }
+        }
+    }
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj) {
         const int j = j_base + jj * kGroups;
@@ -300,23 +327,16 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
             pkeys[h * a.MKBPR + j] =
                 float_key(ldcg_f32(a.probe + (static_cast<size_t>(b) * a.H + n * G + h) * a.MKBPR + j));
         }
+        if (a.importance)
+            for (int j = threadIdx.x; j < nb; j += kThreads)
+                ikeys[j] = float_key(ldcg_f32(a.isum + static_cast<size_t>(u) * a.MKBPR + j));
     } else {
         __syncthreads();
     }
 
     // ---- importance pre-selection (same for every head of the request)
     const int n_imp = a.importance ? min((a.k + 1) / 2, nb) : 0;
-    for (int j = threadIdx.x; j < nb; j += kThreads) {
-        imp_flags[j] = kCand;
-        if (a.importance) {
-            // summed prefill importance of the block, fp32 in token order
-            const int p0 = j * BS, p_end = min(p0 + BS, L);
-            const float* imp = a.importance + static_cast<size_t>(b) * a.imp_stride;
-            float sacc = 0.f;
-            for (int ps = p0; ps < p_end; ++ps) sacc = __fadd_rn(sacc, imp[ps]);
-            ikeys[j] = float_key(sacc);
-        }
-    }
+    for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = kCand;
     __syncthreads();
     if (n_imp > 0) topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
     for (int j = threadIdx.x; j < nb; j += kThreads)
@@ -403,7 +423,9 @@ qs_status launch_g(const ProbeArgs& a, int G, cudaStream_t s) {
 }  // namespace
 
 size_t probe_workspace_bytes(int B, int H, int N, int MKBPR) {
+    // probe scores [B*H, MKBPR], importance sums [B*N, MKBPR], counters [B*N]
     return align_up(static_cast<size_t>(B) * H * MKBPR * 4, 256) +
+           align_up(static_cast<size_t>(B) * N * MKBPR * 4, 256) +
            align_up(static_cast<size_t>(B) * N * 4, 256);
 }
 
@@ -444,7 +466,9 @@ qs_status probe_select_impl(const void* q, qs_dtype q_dtype, const void* k_cache
     a.B = B; a.H = H; a.N = N; a.BS = BS; a.k = k; a.n_probe = n_probe;
     a.selected = selected;
     a.probe = reinterpret_cast<float*>(ws);
-    a.counters = reinterpret_cast<uint32_t*>(ws + align_up(static_cast<size_t>(B) * H * MKBPR * 4, 256));
+    a.isum = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(B) * H * MKBPR * 4, 256));
+    a.counters = reinterpret_cast<uint32_t*>(ws + align_up(static_cast<size_t>(B) * H * MKBPR * 4, 256) +
+                                             align_up(static_cast<size_t>(B) * N * MKBPR * 4, 256));
     a.dev_status = dev_status;
     switch (kv_dtype) {
         case QS_F32: return D == 128 ? launch_g<Dt::F32, 128>(a, G, stream) : launch_g<Dt::F32, 64>(a, G, stream);
