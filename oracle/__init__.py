@@ -28,6 +28,7 @@ def lib():
         _lib = ctypes.CDLL(path)
         P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
         _lib.orc_prefill_metadata.argtypes = [P, I, I, I, I, I, P, I, P, I, P, I, I, P, P]
+        _lib.orc_update_metadata.argtypes = [P, I, I, I, I, I, P, P, I, P, I, P, I, I, P, P]
         _lib.orc_group_mean_query.argtypes = [P, I, I, I, I, I, P]
         _lib.orc_quest_scores.argtypes = [P, P, P, I, P, I, I, P, I, I, I, I, P, P]
         _lib.orc_quest_select.argtypes = [P, I, P, P, I, P, I, I, P, I, I, I, I, I, I, I, P, P]
@@ -37,7 +38,8 @@ def lib():
         _lib.orc_sparse_attention.argtypes = [P, I, P, P, P, P, I, I, P, I, P, P, I, I, D, I, I,
                                               I, I, I, P, P]
         _lib.orc_quantize_query.argtypes = [P, I, I, P, P]
-        for f in ("orc_prefill_metadata", "orc_group_mean_query", "orc_quest_scores",
+        for f in ("orc_prefill_metadata", "orc_update_metadata", "orc_group_mean_query",
+                  "orc_quest_scores",
                   "orc_quest_select", "orc_forced_set", "orc_probe_select",
                   "orc_sparse_attention", "orc_quantize_query"):
             getattr(_lib, f).restype = ctypes.c_int
@@ -76,6 +78,24 @@ def prefill_metadata(k_cache, kv_dt, seq_lens, block_tables, meta_block_tables,
                                     len(seq_lens), _p(bt), bt.shape[1], _p(mbt), mbt.shape[1],
                                     maxblocks.shape[0], _p(maxblocks), _p(minblocks))
     _check(rc, "prefill_metadata")
+    return maxblocks, minblocks
+
+
+def update_metadata(k_cache, kv_dt, prev_lens, seq_lens, block_tables, meta_block_tables,
+                    maxblocks, minblocks):
+    """f1.  Rebuilds, in place, the metadata rows of the blocks touched since
+    the requests held prev_lens tokens (see oracle.h); returns the arrays."""
+    P, BS, N, D = k_cache.shape
+    k_cache = _c(k_cache, _elem_np(kv_dt))
+    prev = _c(prev_lens, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    bt = _c(block_tables, np.int32)
+    mbt = _c(meta_block_tables, np.int32)
+    assert maxblocks.flags.c_contiguous and minblocks.flags.c_contiguous
+    rc = lib().orc_update_metadata(_p(k_cache), kv_dt, P, BS, N, D, _p(prev), _p(seq_lens),
+                                   len(seq_lens), _p(bt), bt.shape[1], _p(mbt), mbt.shape[1],
+                                   maxblocks.shape[0], _p(maxblocks), _p(minblocks))
+    _check(rc, "update_metadata")
     return maxblocks, minblocks
 
 

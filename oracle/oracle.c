@@ -73,6 +73,71 @@ static int less_total(double a, double b) {
     return 0;
 }
 
+/* One metadata row: for KV block j of request b, the channel-wise max and min
+ * over its valid tokens (or a zero row when j >= nb), written at row r of
+ * meta block m.  Returns ORC_ERANGE for a bad block-table entry. */
+static int meta_row(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, int N, int D,
+                    int L, int nb, const int32_t* bt_row, int j, int m, int r,
+                    void* maxblocks, void* minblocks) {
+    const size_t es = esize(kv_dt);
+    const size_t row = (size_t)N * D; /* elements of one token (all heads) */
+    const size_t out_row = ((size_t)m * BS + r) * row;
+    if (j >= nb) {
+        /* absent KV block: zero metadata ('tail zero fill') */
+        memset((char*)maxblocks + out_row * es, 0, row * es);
+        memset((char*)minblocks + out_row * es, 0, row * es);
+        return ORC_OK;
+    }
+    const int p = bt_row[j];
+    if (p < 0 || p >= num_kv_blocks) return ORC_ERANGE;
+    int valid = L - j * BS;
+    if (valid > BS) valid = BS;
+    for (int n = 0; n < N; n++) {
+        for (int d = 0; d < D; d++) {
+            /* channel-wise reduce over the block's valid tokens */
+            size_t imax = ((size_t)p * BS) * row + (size_t)n * D + d;
+            size_t imin = imax;
+            double vmax = dec(k_cache, kv_dt, imax), vmin = vmax;
+            for (int t = 1; t < valid; t++) {
+                size_t i = ((size_t)p * BS + t) * row + (size_t)n * D + d;
+                double v = dec(k_cache, kv_dt, i);
+                if (less_total(vmax, v)) { vmax = v; imax = i; }
+                if (less_total(v, vmin)) { vmin = v; imin = i; }
+            }
+            size_t o = out_row + (size_t)n * D + d;
+            memcpy((char*)maxblocks + o * es, (const char*)k_cache + imax * es, es);
+            memcpy((char*)minblocks + o * es, (const char*)k_cache + imin * es, es);
+        }
+    }
+    return ORC_OK;
+}
+
+/* Rows [first_block[b], n_meta * BS) of every request (first_block NULL: all
+ * rows of the used meta blocks). */
+static int metadata_rows(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, int N, int D,
+                         const int32_t* first_block, const int32_t* seq_lens, int B,
+                         const int32_t* block_tables, int MKBPR,
+                         const int32_t* meta_block_tables, int MMBPR, int num_meta_blocks,
+                         void* maxblocks, void* minblocks) {
+    for (int b = 0; b < B; b++) {
+        const int L = seq_lens[b];
+        if (L < 0 || L > MKBPR * BS) return ORC_EINVAL;
+        const int nb = ceil_div(L, BS);
+        const int n_meta = ceil_div(nb, BS);
+        if (n_meta > MMBPR) return ORC_EINVAL;
+        const int j0 = first_block ? first_block[b] : 0;
+        for (int j = j0; j < n_meta * BS; j++) {
+            const int m = meta_block_tables[(size_t)b * MMBPR + j / BS];
+            if (m < 0 || m >= num_meta_blocks) return ORC_ERANGE;
+            const int rc = meta_row(k_cache, kv_dt, num_kv_blocks, BS, N, D, L, nb,
+                                    block_tables + (size_t)b * MKBPR, j, m, j % BS, maxblocks,
+                                    minblocks);
+            if (rc != ORC_OK) return rc;
+        }
+    }
+    return ORC_OK;
+}
+
 int orc_prefill_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int BS,
                          int N, int D, const int32_t* seq_lens, int B,
                          const int32_t* block_tables, int MKBPR,
@@ -81,51 +146,39 @@ int orc_prefill_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int 
     if (!is_float_dt(kv_dt) || BS <= 0 || N <= 0 || D <= 0 || B < 0 || MKBPR < 0 ||
         MMBPR < 0)
         return ORC_EINVAL;
-    const size_t es = esize(kv_dt);
-    const size_t row = (size_t)N * D; /* elements of one token (all heads) */
+    return metadata_rows(k_cache, kv_dt, num_kv_blocks, BS, N, D, NULL, seq_lens, B,
+                         block_tables, MKBPR, meta_block_tables, MMBPR, num_meta_blocks,
+                         maxblocks, minblocks);
+}
+
+/* f1: incremental update after decoding.  The metadata was last built (or
+ * updated) at lengths prev_lens; the requests now hold seq_lens tokens.  The
+ * block that held the last tokens then (possibly partial) and every block
+ * begun since are rebuilt, and rows past the new block count inside the used
+ * meta blocks are zeroed; every other row is left as it is.  So prefill at
+ * prev_lens followed by this update equals prefill at seq_lens. */
+int orc_update_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, int N, int D,
+                        const int32_t* prev_lens, const int32_t* seq_lens, int B,
+                        const int32_t* block_tables, int MKBPR,
+                        const int32_t* meta_block_tables, int MMBPR, int num_meta_blocks,
+                        void* maxblocks, void* minblocks) {
+    if (!is_float_dt(kv_dt) || BS <= 0 || N <= 0 || D <= 0 || B < 0 || MKBPR < 0 ||
+        MMBPR < 0 || !prev_lens)
+        return ORC_EINVAL;
+    int32_t* first = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    if (!first) return ORC_EINVAL;
     for (int b = 0; b < B; b++) {
-        const int L = seq_lens[b];
-        if (L < 0 || L > MKBPR * BS) return ORC_EINVAL;
-        const int nb = ceil_div(L, BS);
-        const int n_meta = ceil_div(nb, BS);
-        if (n_meta > MMBPR) return ORC_EINVAL;
-        for (int ms = 0; ms < n_meta; ms++) {
-            const int m = meta_block_tables[(size_t)b * MMBPR + ms];
-            if (m < 0 || m >= num_meta_blocks) return ORC_ERANGE;
-            for (int r = 0; r < BS; r++) {
-                const int j = ms * BS + r; /* in-sequence KV block */
-                const size_t out_row = ((size_t)m * BS + r) * row;
-                if (j >= nb) {
-                    /* absent KV block: zero metadata ('tail zero fill') */
-                    memset((char*)maxblocks + out_row * es, 0, row * es);
-                    memset((char*)minblocks + out_row * es, 0, row * es);
-                    continue;
-                }
-                const int p = block_tables[(size_t)b * MKBPR + j];
-                if (p < 0 || p >= num_kv_blocks) return ORC_ERANGE;
-                int valid = L - j * BS;
-                if (valid > BS) valid = BS;
-                for (int n = 0; n < N; n++) {
-                    for (int d = 0; d < D; d++) {
-                        /* channel-wise reduce over the block's valid tokens */
-                        size_t imax = ((size_t)p * BS) * row + (size_t)n * D + d;
-                        size_t imin = imax;
-                        double vmax = dec(k_cache, kv_dt, imax), vmin = vmax;
-                        for (int t = 1; t < valid; t++) {
-                            size_t i = ((size_t)p * BS + t) * row + (size_t)n * D + d;
-                            double v = dec(k_cache, kv_dt, i);
-                            if (less_total(vmax, v)) { vmax = v; imax = i; }
-                            if (less_total(v, vmin)) { vmin = v; imin = i; }
-                        }
-                        size_t o = out_row + (size_t)n * D + d;
-                        memcpy((char*)maxblocks + o * es, (const char*)k_cache + imax * es, es);
-                        memcpy((char*)minblocks + o * es, (const char*)k_cache + imin * es, es);
-                    }
-                }
-            }
+        if (prev_lens[b] < 0 || prev_lens[b] > seq_lens[b]) {
+            free(first);
+            return ORC_EINVAL;
         }
+        first[b] = prev_lens[b] / BS;
     }
-    return ORC_OK;
+    const int rc = metadata_rows(k_cache, kv_dt, num_kv_blocks, BS, N, D, first, seq_lens, B,
+                                 block_tables, MKBPR, meta_block_tables, MMBPR, num_meta_blocks,
+                                 maxblocks, minblocks);
+    free(first);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */

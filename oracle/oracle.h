@@ -46,6 +46,18 @@ int orc_prefill_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int 
                          const int32_t* meta_block_tables, int MMBPR,
                          int num_meta_blocks, void* maxblocks, void* minblocks);
 
+/* Incremental metadata update after decoding (f1): with the metadata last
+ * built at lengths prev_lens, rebuilds the rows of blocks
+ * [prev_lens[b] / BS, ceil(seq_lens[b] / BS)) and zeroes the rows past the new
+ * block count inside the used meta blocks; other rows are untouched.
+ * Prefill at prev_lens then this update equals prefill at seq_lens.
+ * ORC_EINVAL when prev_lens[b] < 0 or > seq_lens[b]. */
+int orc_update_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, int N, int D,
+                        const int32_t* prev_lens, const int32_t* seq_lens, int B,
+                        const int32_t* block_tables, int MKBPR,
+                        const int32_t* meta_block_tables, int MMBPR, int num_meta_blocks,
+                        void* maxblocks, void* minblocks);
+
 /* Group-mean query (a2): qg[b][n][d] = mean over the H/N query heads of group n. */
 int orc_group_mean_query(const void* q, int q_dt, int B, int H, int N, int D,
                          double* qg);

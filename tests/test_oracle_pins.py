@@ -90,6 +90,68 @@ def test_metadata_rejects_bad_table_entry():
 
 
 # --------------------------------------------------------------------------
+# f1 incremental metadata update
+# --------------------------------------------------------------------------
+
+UPD_PREV, UPD_NEW = (0, 3, 13, 8), (0, 9, 21, 8)   # BS=4: empty, in-block, new meta block, no growth
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_metadata_update_rows_against_torch(dtype):
+    """Rows of blocks [prev // BS, ceil(L / BS)) hold the amax/amin of the
+    blocks' valid tokens at the new lengths, rows past the block count inside
+    the used meta blocks are zero, and every row below prev // BS keeps what
+    it held (planted values, not recomputed)."""
+    BS = 4
+    k, bt, mbt, sl, M = ragged_case(dtype, B=4, BS=BS, seq_lens=UPD_NEW, MKBPR=6, MMBPR=2)
+    N, D = k.shape[2], k.shape[3]
+    prev = torch.tensor(UPD_PREV, dtype=torch.int32)
+    planted = torch.full((M, BS, N, D), 3.0, dtype=dtype)
+    mx, mn = to_np(planted).copy(), to_np(planted).copy()
+    oracle.update_metadata(to_np(k), odt(k), to_np(prev), to_np(sl), to_np(bt), to_np(mbt), mx, mn)
+    mx_t, mn_t = from_bits(mx, dtype), from_bits(mn, dtype)
+    for b, (P0, L) in enumerate(zip(UPD_PREV, UPD_NEW)):
+        nb = (L + BS - 1) // BS
+        for j in range(((nb + BS - 1) // BS) * BS):
+            m, r = int(mbt[b, j // BS]), j % BS
+            if j < P0 // BS:
+                assert torch.all(mx_t[m, r] == 3.0) and torch.all(mn_t[m, r] == 3.0), (b, j)
+            elif j >= nb:
+                assert torch.all(mx_t[m, r] == 0) and torch.all(mn_t[m, r] == 0), (b, j)
+            else:
+                toks = k[int(bt[b, j]), :min(BS, L - j * BS)].float()
+                assert torch.equal(mx_t[m, r].float(), torch.amax(toks, dim=0)), (b, j)
+                assert torch.equal(mn_t[m, r].float(), torch.amin(toks, dim=0)), (b, j)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_metadata_update_after_prefill_equals_prefill_at_new_lengths(dtype):
+    BS = 4
+    k, bt, mbt, sl, M = ragged_case(dtype, seed=3, B=4, BS=BS, seq_lens=UPD_NEW, MKBPR=6, MMBPR=2)
+    N, D = k.shape[2], k.shape[3]
+    prev = np.array(UPD_PREV, np.int32)
+    sent = to_np(torch.full((M, BS, N, D), 7.0, dtype=dtype))
+    mx, mn = sent.copy(), sent.copy()
+    oracle.prefill_metadata(to_np(k), odt(k), prev, to_np(bt), to_np(mbt), mx, mn)
+    oracle.update_metadata(to_np(k), odt(k), prev, to_np(sl), to_np(bt), to_np(mbt), mx, mn)
+    fx, fn = sent.copy(), sent.copy()
+    oracle.prefill_metadata(to_np(k), odt(k), to_np(sl), to_np(bt), to_np(mbt), fx, fn)
+    assert np.array_equal(mx, fx) and np.array_equal(mn, fn)
+    # idempotent: an update with no new token rebuilds the partial last block only
+    oracle.update_metadata(to_np(k), odt(k), to_np(sl), to_np(sl), to_np(bt), to_np(mbt), mx, mn)
+    assert np.array_equal(mx, fx) and np.array_equal(mn, fn)
+
+
+def test_metadata_update_rejects_shrinking_lengths():
+    k, bt, mbt, sl, M = ragged_case(torch.float32, B=4, seq_lens=UPD_NEW, MKBPR=6, MMBPR=2)
+    mx = np.zeros((M, 4, 2, 5), np.float32)
+    prev = np.array([0, 10, 13, 8], np.int32)          # 10 > 9
+    with pytest.raises(oracle.OracleError):
+        oracle.update_metadata(to_np(k), oracle.F32, prev, to_np(sl), to_np(bt), to_np(mbt), mx,
+                               mx.copy())
+
+
+# --------------------------------------------------------------------------
 # a2, a3: group mean and Quest score
 # --------------------------------------------------------------------------
 
