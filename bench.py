@@ -259,6 +259,43 @@ def setup(w, seed, dev, fused_select=-1, seq_lens=None):
     return x, mode, sel, out, params, meta_ms
 
 
+def metadata_update(w, x, dev, flush, sink, reps=5):
+    """Times the incremental metadata update for one decoded block per request
+    (the metadata is refreshed every BS tokens): rows rebuilt since
+    prev = meta_len - BS, one update after an L2 flush per sample.  Returns
+    (median us, bytes: K read for the touched blocks + rows written)."""
+    from decode_sparse_attention_gb300 import questsparse as qs
+    L = x["meta_seq_lens"]
+    prev = torch.clamp(L - w.BS, min=0).to(torch.int32)
+    args = (x["k_cache"], prev, L, x["block_tables"], x["meta_block_tables"], x["maxblocks"],
+            x["minblocks"])
+    for _ in range(2):
+        qs.quest_update_metadata(*args)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        flush_l2(flush, sink)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        qs.quest_update_metadata(*args)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(1000.0 * e0.elapsed_time(e1))
+    es = elem_bytes(x["k_cache"].dtype)
+    row = w.N * w.D * es
+    nbytes = 0
+    for p0, l in zip(prev.cpu().tolist(), L.cpu().tolist()):
+        nb = (l + w.BS - 1) // w.BS
+        rows = (nb + w.BS - 1) // w.BS * w.BS
+        zero_from = max(nb, ((p0 + w.BS - 1) // w.BS + w.BS - 1) // w.BS * w.BS)
+        for j in range(p0 // w.BS, rows):
+            if j < nb:
+                nbytes += min(w.BS, l - j * w.BS) * row + 2 * row
+            elif j >= zero_from:
+                nbytes += 2 * row
+    return statistics.median(times), nbytes
+
+
 def flush_l2(flush, sink):
     """Evict the L2: write a buffer twice the L2 size, then read it back, so
     the next kernel starts with none of its inputs cached and no dirty lines
@@ -491,6 +528,11 @@ def run_ours(args, w):
         "gpu_launches": kernels * args.steps,
     }
     if meta_ms is not None:
+        upd_us, upd_bytes = metadata_update(w, x0, dev, flush, sink)
+        res["metadata_update_us"] = round(upd_us, 2)
+        res["metadata_update_gbs"] = round(upd_bytes / (upd_us * 1e-6) / 1e9, 1)
+        res["metadata_update"] = ("one decoded block per request: rows rebuilt since "
+                                  "meta_len - BS, one update after an L2 flush, %d bytes" % upd_bytes)
         L = x0["meta_seq_lens"].cpu().numpy()
         kbytes = int(sum(int(l) for l in L)) * w.N * w.D * elem_bytes(x0["k_cache"].dtype)
         mrows = sum(((int(l) + w.BS - 1) // w.BS + w.BS - 1) // w.BS * w.BS

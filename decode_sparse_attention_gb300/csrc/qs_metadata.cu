@@ -14,7 +14,6 @@
 namespace qs {
 namespace {
 
-constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
 
 // Integer-ordered view of a float element: key(-x) < key(+0) < key(x>0).  The
@@ -77,10 +76,14 @@ QS_DEVINL uint4 from_keys(uint4 k) {
     return make_uint4(K::to_key(k.x), K::to_key(k.y), K::to_key(k.z), K::to_key(k.w));
 }
 
-template <Dt T>
-__global__ void __launch_bounds__(kThreads)
+// NT threads: 256 for the prefill (many items per launch), 1024 for the
+// incremental update (a few rows per request, so each row gets more token
+// groups in flight).
+template <Dt T, int NT>
+__global__ void __launch_bounds__(NT)
 prefill_metadata_kernel(const uint8_t* __restrict__ k_cache, int num_kv_blocks, int BS, int vpr,
-                        const int32_t* __restrict__ seq_lens, int B,
+                        const int32_t* __restrict__ prev_lens, const int32_t* __restrict__ seq_lens,
+                        int B,
                         const int32_t* __restrict__ block_tables, int MKBPR,
                         const int32_t* __restrict__ meta_tables, int MMBPR, int num_meta,
                         uint8_t* __restrict__ maxblocks, uint8_t* __restrict__ minblocks,
@@ -88,47 +91,47 @@ prefill_metadata_kernel(const uint8_t* __restrict__ k_cache, int num_kv_blocks, 
     using K = KeyOps<T>;
     extern __shared__ uint4 smem[];  // [groups][vpr] max, then [groups][vpr] min
     const size_t row_bytes = static_cast<size_t>(vpr) * 16;
-    const int groups = vpr >= kThreads ? 1 : kThreads / vpr;
+    const int groups = vpr >= NT ? 1 : NT / vpr;
     uint4* s_max = smem;
-    uint4* s_min = smem + static_cast<size_t>(groups) * min(vpr, kThreads);
+    uint4* s_min = smem + static_cast<size_t>(groups) * min(vpr, NT);
     const int slots = MMBPR * BS;
     const long long items = static_cast<long long>(B) * slots;
 
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-        const int b = static_cast<int>(it / slots);
-        const int j = static_cast<int>(it % slots);
+    // one (request, in-sequence block slot) item: reduce the block or zero
+    // its row; returns early where the item needs nothing
+    auto item = [&](int b, int j) {
         const int L = seq_lens[b];
         if (L < 0 || L > MKBPR * BS) {
             if (j == 0 && threadIdx.x == 0) set_status(dev_status, QS_DEV_ESEQ_LEN);
-            continue;
+            return;
         }
         const int nb = (L + BS - 1) / BS;
         const int n_meta = (nb + BS - 1) / BS;
-        if (j >= n_meta * BS) continue;  // metadata slot the request does not use
+        if (j >= n_meta * BS) return;  // metadata slot the request does not use
         const int m = meta_tables[static_cast<size_t>(b) * MMBPR + j / BS];
         if (m < 0 || m >= num_meta) {
             if (threadIdx.x == 0) set_status(dev_status, QS_DEV_EMETA_TABLE);
-            continue;
+            return;
         }
         const size_t out_off = (static_cast<size_t>(m) * BS + j % BS) * row_bytes;
         if (j >= nb) {  // block beyond the sequence: zero row (all heads)
-            for (int v = threadIdx.x; v < vpr; v += kThreads) {
+            for (int v = threadIdx.x; v < vpr; v += NT) {
                 stg_v4(maxblocks + out_off + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
                 stg_v4(minblocks + out_off + static_cast<size_t>(v) * 16, make_uint4(0, 0, 0, 0));
             }
-            continue;
+            return;
         }
         const int p = block_tables[static_cast<size_t>(b) * MKBPR + j];
         if (p < 0 || p >= num_kv_blocks) {
             if (threadIdx.x == 0) set_status(dev_status, QS_DEV_EBLOCK_TABLE);
-            continue;
+            return;
         }
         const int valid = min(BS, L - j * BS);
         const uint8_t* blk = k_cache + static_cast<size_t>(p) * BS * row_bytes;
 
-        for (int v0 = 0; v0 < vpr; v0 += kThreads) {
+        for (int v0 = 0; v0 < vpr; v0 += NT) {
             // thread -> (token group g, vector v) for this slice of the row
-            const int span = min(vpr - v0, kThreads);
+            const int span = min(vpr - v0, NT);
             const int g = groups > 1 ? threadIdx.x / vpr : 0;
             const int v = groups > 1 ? threadIdx.x % vpr : threadIdx.x;
             const bool active = v < span && g < groups;
@@ -171,7 +174,29 @@ prefill_metadata_kernel(const uint8_t* __restrict__ k_cache, int num_kv_blocks, 
                 stg_v4(minblocks + o, from_keys<T>(mn));
             }
         }
+        };
+    if (prev_lens) {
+        // incremental update: per request, the rows of the blocks touched
+        // since prev_lens (the block that held the last tokens and every
+        // block begun since) and the zero rows of meta blocks begun since
+        // (rows past the block count in meta blocks already in use are zero
+        // from the earlier build)
+        for (int b = blockIdx.x; b < B; b += gridDim.x) {
+            const int L = seq_lens[b], P0 = prev_lens[b];
+            if (L < 0 || L > MKBPR * BS || P0 < 0 || P0 > L) {
+                if (threadIdx.x == 0) set_status(dev_status, QS_DEV_ESEQ_LEN);
+                continue;
+            }
+            const int nb = (L + BS - 1) / BS;
+            const int rows = (nb + BS - 1) / BS * BS;
+            const int zero_from = max(nb, ((P0 + BS - 1) / BS + BS - 1) / BS * BS);
+            for (int j = P0 / BS; j < rows; ++j)
+                if (j < nb || j >= zero_from) item(b, j);
+        }
+        return;
     }
+    for (long long it = blockIdx.x; it < items; it += gridDim.x)
+        item(static_cast<int>(it / slots), static_cast<int>(it % slots));
 }
 
 }  // namespace
@@ -179,9 +204,9 @@ prefill_metadata_kernel(const uint8_t* __restrict__ k_cache, int num_kv_blocks, 
 
 using namespace qs;
 
-extern "C" qs_status qs_prefill_metadata(const void* k_cache, qs_dtype kv_dtype,
-                                         int32_t num_kv_blocks, int32_t BS, int32_t N,
-                                         int32_t D, const int32_t* seq_lens, int32_t B,
+static qs_status metadata_impl(const void* k_cache, qs_dtype kv_dtype, int32_t num_kv_blocks,
+                               int32_t BS, int32_t N, int32_t D, const int32_t* prev_lens,
+                               const int32_t* seq_lens, int32_t B,
                                          const int32_t* block_tables, int32_t MKBPR,
                                          const int32_t* meta_block_tables, int32_t MMBPR,
                                          int32_t num_meta_blocks, void* maxblocks,
@@ -207,9 +232,10 @@ extern "C" qs_status qs_prefill_metadata(const void* k_cache, qs_dtype kv_dtype,
          reinterpret_cast<uintptr_t>(minblocks)) % 16 != 0)
         return QS_EINVAL;
     const int vpr = static_cast<int>(row_bytes / 16);
-    const int groups = vpr >= 256 ? 1 : 256 / vpr;
-    const size_t smem = static_cast<size_t>(groups) * (vpr < 256 ? vpr : 256) * 16 * 2;
-    const long long items = static_cast<long long>(B) * MMBPR * BS;
+    const int nt = prev_lens ? 1024 : 256;
+    const int groups = vpr >= nt ? 1 : nt / vpr;
+    const size_t smem = static_cast<size_t>(groups) * (vpr < nt ? vpr : nt) * 16 * 2;
+    const long long items = prev_lens ? B : static_cast<long long>(B) * MMBPR * BS;
     long long grid = static_cast<long long>(num_sms()) * 4;
     if (grid > items) grid = items;
     if (grid < 1) grid = 1;
@@ -217,19 +243,54 @@ extern "C" qs_status qs_prefill_metadata(const void* k_cache, qs_dtype kv_dtype,
     auto args = [&](auto kern) {
         if (smem > 48 * 1024 && !ensure_smem(reinterpret_cast<const void*>(kern), smem))
             return false;
-        kern<<<static_cast<unsigned>(grid), 256, smem, s>>>(
-            static_cast<const uint8_t*>(k_cache), num_kv_blocks, BS, vpr, seq_lens, B,
+        kern<<<static_cast<unsigned>(grid), nt, smem, s>>>(
+            static_cast<const uint8_t*>(k_cache), num_kv_blocks, BS, vpr, prev_lens, seq_lens, B,
             block_tables, MKBPR, meta_block_tables, MMBPR, num_meta_blocks,
             static_cast<uint8_t*>(maxblocks), static_cast<uint8_t*>(minblocks), dev_status);
         return true;
     };
     bool ok;
-    switch (kv_dtype) {
-        case QS_F32: ok = args(prefill_metadata_kernel<Dt::F32>); break;
-        case QS_BF16: ok = args(prefill_metadata_kernel<Dt::BF16>); break;
-        default: ok = args(prefill_metadata_kernel<Dt::F16>); break;
+    if (prev_lens) {
+        switch (kv_dtype) {
+            case QS_F32: ok = args(prefill_metadata_kernel<Dt::F32, 1024>); break;
+            case QS_BF16: ok = args(prefill_metadata_kernel<Dt::BF16, 1024>); break;
+            default: ok = args(prefill_metadata_kernel<Dt::F16, 1024>); break;
+        }
+    } else {
+        switch (kv_dtype) {
+            case QS_F32: ok = args(prefill_metadata_kernel<Dt::F32, 256>); break;
+            case QS_BF16: ok = args(prefill_metadata_kernel<Dt::BF16, 256>); break;
+            default: ok = args(prefill_metadata_kernel<Dt::F16, 256>); break;
+        }
     }
     if (!ok) return QS_ECUDA;
     QS_CHECK_LAUNCH();
     return QS_OK;
+}
+
+extern "C" qs_status qs_prefill_metadata(const void* k_cache, qs_dtype kv_dtype,
+                                         int32_t num_kv_blocks, int32_t BS, int32_t N,
+                                         int32_t D, const int32_t* seq_lens, int32_t B,
+                                         const int32_t* block_tables, int32_t MKBPR,
+                                         const int32_t* meta_block_tables, int32_t MMBPR,
+                                         int32_t num_meta_blocks, void* maxblocks,
+                                         void* minblocks, int32_t* dev_status,
+                                         qs_stream_t stream) {
+    return metadata_impl(k_cache, kv_dtype, num_kv_blocks, BS, N, D, nullptr, seq_lens, B,
+                         block_tables, MKBPR, meta_block_tables, MMBPR, num_meta_blocks,
+                         maxblocks, minblocks, dev_status, stream);
+}
+
+extern "C" qs_status qs_update_metadata(const void* k_cache, qs_dtype kv_dtype,
+                                        int32_t num_kv_blocks, int32_t BS, int32_t N, int32_t D,
+                                        const int32_t* prev_lens, const int32_t* seq_lens,
+                                        int32_t B, const int32_t* block_tables, int32_t MKBPR,
+                                        const int32_t* meta_block_tables, int32_t MMBPR,
+                                        int32_t num_meta_blocks, void* maxblocks,
+                                        void* minblocks, int32_t* dev_status,
+                                        qs_stream_t stream) {
+    if (!prev_lens) return QS_EINVAL;
+    return metadata_impl(k_cache, kv_dtype, num_kv_blocks, BS, N, D, prev_lens, seq_lens, B,
+                         block_tables, MKBPR, meta_block_tables, MMBPR, num_meta_blocks,
+                         maxblocks, minblocks, dev_status, stream);
 }

@@ -70,6 +70,8 @@ def lib():
                                             ctypes.POINTER(SZ)]
             L.qs_prefill_metadata.argtypes = [P, I32, I32, I32, I32, I32, P, I32, P, I32, P, I32,
                                               I32, P, P, P, P]
+            L.qs_update_metadata.argtypes = [P, I32, I32, I32, I32, I32, P, P, I32, P, I32, P,
+                                             I32, I32, P, P, P, P]
             L.qs_block_select_paged.argtypes = [P, I32, P, P, I32, P, I32, I32, P, I32, I32, I32,
                                                 I32, I32, I32, I32, P, P, P, SZ, P, P]
             L.qs_probe_select.argtypes = [P, I32, P, P, I32, I32, P, I32, P, P, I32, I32, I32,
@@ -201,6 +203,33 @@ def quest_prefill_metadata(k_cache, seq_lens, block_tables, metadata_block_table
                                    maxblocks.shape[0], _ptr(maxblocks), _ptr(minblocks),
                                    _ptr(status_word(k_cache.device)), _stream(k_cache.device))
     _check(rc, "qs_prefill_metadata")
+
+
+def quest_update_metadata(k_cache, prev_lens, seq_lens, block_tables, metadata_block_tables,
+                          maxblocks, minblocks):
+    """Refreshes maxblocks/minblocks after decoding: rebuilds the rows of the
+    blocks touched since the requests held prev_lens tokens (the block that
+    held the last tokens and every block begun since) and zeroes the tail rows
+    of metadata blocks begun since, leaving the rest."""
+    _req(k_cache, "k_cache", dim=4)
+    P_, BS, N, D = k_cache.shape
+    _req(prev_lens, "prev_lens", torch.int32, 1)
+    _req(seq_lens, "seq_lens", torch.int32, 1)
+    _req(block_tables, "block_tables", torch.int32, 2)
+    _req(metadata_block_tables, "metadata_block_tables", torch.int32, 2)
+    for t, nm in ((maxblocks, "maxblocks"), (minblocks, "minblocks")):
+        _req(t, nm, k_cache.dtype, 4)
+        if tuple(t.shape[1:]) != (BS, N, D):
+            raise QuestSparseError("%s must be [num_meta, BS, N, D]" % nm)
+    B = seq_lens.shape[0]
+    if prev_lens.shape[0] != B:
+        raise QuestSparseError("prev_lens and seq_lens must have one entry per request")
+    rc = lib().qs_update_metadata(_ptr(k_cache), _dt(k_cache), P_, BS, N, D, _ptr(prev_lens),
+                                  _ptr(seq_lens), B, _ptr(block_tables), block_tables.shape[1],
+                                  _ptr(metadata_block_tables), metadata_block_tables.shape[1],
+                                  maxblocks.shape[0], _ptr(maxblocks), _ptr(minblocks),
+                                  _ptr(status_word(k_cache.device)), _stream(k_cache.device))
+    _check(rc, "qs_update_metadata")
 
 
 def quest_block_select_paged_in_out_w(query, maxblocks, minblocks, metadata_block_tables,

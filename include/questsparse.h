@@ -4,6 +4,7 @@
  *
  * Operations and where they are defined:
  *   qs_prefill_metadata    CANN ops-transformer select_attention_operators page
+ *   qs_update_metadata     the same page (metadata refreshed while decoding)
  *                          (Quest on Ascend 910B), section 'quest_prefill_metadata:
  *                          metadata construction'.
  *   qs_block_select_paged  same page, section 'quest_block_select_paged: decode-time
@@ -131,6 +132,30 @@ qs_status qs_prefill_metadata(const void* k_cache, qs_dtype kv_dtype, int32_t nu
                               const int32_t* meta_block_tables, int32_t MMBPR,
                               int32_t num_meta_blocks, void* maxblocks, void* minblocks,
                               int32_t* dev_status, qs_stream_t stream);
+
+/*
+ * Incremental Quest metadata update after decoding (the CANN page's
+ * tokens_since_metadata_update: the metadata is refreshed every BS decoded
+ * tokens).  The metadata was last built or updated when request b held
+ * prev_lens[b] tokens; it now holds seq_lens[b].  Rebuilds, as
+ * qs_prefill_metadata would, the rows of blocks prev_lens[b]/BS ..
+ * ceil(seq_lens[b]/BS) - 1 (the block that held the last tokens, possibly
+ * partial, and every block begun since) and zero-fills the rows past the new
+ * block count inside the metadata blocks begun since prev_lens (rows past the
+ * block count in metadata blocks already in use were zeroed by the earlier
+ * build); no other row is read or written.  Hence qs_prefill_metadata at
+ * prev_lens followed by this call leaves exactly what qs_prefill_metadata at
+ * seq_lens writes, at a cost proportional to the tokens added.
+ * prev_lens: device int32 [B].  A request with prev_lens[b] < 0 or
+ * prev_lens[b] > seq_lens[b] is skipped with QS_DEV_ESEQ_LEN.  Other arguments
+ * and errors as for qs_prefill_metadata; NULL prev_lens: QS_EINVAL.
+ */
+qs_status qs_update_metadata(const void* k_cache, qs_dtype kv_dtype, int32_t num_kv_blocks,
+                             int32_t BS, int32_t N, int32_t D, const int32_t* prev_lens,
+                             const int32_t* seq_lens, int32_t B, const int32_t* block_tables,
+                             int32_t MKBPR, const int32_t* meta_block_tables, int32_t MMBPR,
+                             int32_t num_meta_blocks, void* maxblocks, void* minblocks,
+                             int32_t* dev_status, qs_stream_t stream);
 
 /*
  * Quest block selection (CANN page, 'quest_block_select_paged', steps 1-3).

@@ -112,10 +112,12 @@ static int meta_row(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, i
     return ORC_OK;
 }
 
-/* Rows [first_block[b], n_meta * BS) of every request (first_block NULL: all
- * rows of the used meta blocks). */
+/* For every request: blocks [first_block[b], nb) are rebuilt and the zero
+ * rows [max(nb, zero_from[b]), n_meta * BS) written (NULL arrays: from 0, i.e.
+ * every row of the used meta blocks). */
 static int metadata_rows(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, int N, int D,
-                         const int32_t* first_block, const int32_t* seq_lens, int B,
+                         const int32_t* first_block, const int32_t* zero_from,
+                         const int32_t* seq_lens, int B,
                          const int32_t* block_tables, int MKBPR,
                          const int32_t* meta_block_tables, int MMBPR, int num_meta_blocks,
                          void* maxblocks, void* minblocks) {
@@ -126,7 +128,9 @@ static int metadata_rows(const void* k_cache, int kv_dt, int num_kv_blocks, int 
         const int n_meta = ceil_div(nb, BS);
         if (n_meta > MMBPR) return ORC_EINVAL;
         const int j0 = first_block ? first_block[b] : 0;
+        const int z0 = zero_from ? (zero_from[b] > nb ? zero_from[b] : nb) : nb;
         for (int j = j0; j < n_meta * BS; j++) {
+            if (j >= nb && j < z0) continue;   /* already zero */
             const int m = meta_block_tables[(size_t)b * MMBPR + j / BS];
             if (m < 0 || m >= num_meta_blocks) return ORC_ERANGE;
             const int rc = meta_row(k_cache, kv_dt, num_kv_blocks, BS, N, D, L, nb,
@@ -146,7 +150,7 @@ int orc_prefill_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int 
     if (!is_float_dt(kv_dt) || BS <= 0 || N <= 0 || D <= 0 || B < 0 || MKBPR < 0 ||
         MMBPR < 0)
         return ORC_EINVAL;
-    return metadata_rows(k_cache, kv_dt, num_kv_blocks, BS, N, D, NULL, seq_lens, B,
+    return metadata_rows(k_cache, kv_dt, num_kv_blocks, BS, N, D, NULL, NULL, seq_lens, B,
                          block_tables, MKBPR, meta_block_tables, MMBPR, num_meta_blocks,
                          maxblocks, minblocks);
 }
@@ -154,9 +158,11 @@ int orc_prefill_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int 
 /* f1: incremental update after decoding.  The metadata was last built (or
  * updated) at lengths prev_lens; the requests now hold seq_lens tokens.  The
  * block that held the last tokens then (possibly partial) and every block
- * begun since are rebuilt, and rows past the new block count inside the used
- * meta blocks are zeroed; every other row is left as it is.  So prefill at
- * prev_lens followed by this update equals prefill at seq_lens. */
+ * begun since are rebuilt, and the rows past the new block count inside the
+ * meta blocks begun since are zeroed (rows past the block count inside meta
+ * blocks already in use were zeroed by the earlier build); every other row is
+ * left as it is.  So prefill at prev_lens followed by this update equals
+ * prefill at seq_lens. */
 int orc_update_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, int N, int D,
                         const int32_t* prev_lens, const int32_t* seq_lens, int B,
                         const int32_t* block_tables, int MKBPR,
@@ -165,18 +171,20 @@ int orc_update_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int B
     if (!is_float_dt(kv_dt) || BS <= 0 || N <= 0 || D <= 0 || B < 0 || MKBPR < 0 ||
         MMBPR < 0 || !prev_lens)
         return ORC_EINVAL;
-    int32_t* first = (int32_t*)malloc(sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+    int32_t* first = (int32_t*)malloc(sizeof(int32_t) * 2 * (size_t)(B > 0 ? B : 1));
     if (!first) return ORC_EINVAL;
+    int32_t* zfrom = first + (B > 0 ? B : 1);
     for (int b = 0; b < B; b++) {
         if (prev_lens[b] < 0 || prev_lens[b] > seq_lens[b]) {
             free(first);
             return ORC_EINVAL;
         }
         first[b] = prev_lens[b] / BS;
+        zfrom[b] = ceil_div(ceil_div(prev_lens[b], BS), BS) * BS;  /* end of meta blocks in use */
     }
-    const int rc = metadata_rows(k_cache, kv_dt, num_kv_blocks, BS, N, D, first, seq_lens, B,
-                                 block_tables, MKBPR, meta_block_tables, MMBPR, num_meta_blocks,
-                                 maxblocks, minblocks);
+    const int rc = metadata_rows(k_cache, kv_dt, num_kv_blocks, BS, N, D, first, zfrom, seq_lens,
+                                 B, block_tables, MKBPR, meta_block_tables, MMBPR,
+                                 num_meta_blocks, maxblocks, minblocks);
     free(first);
     return rc;
 }

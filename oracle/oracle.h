@@ -49,7 +49,8 @@ int orc_prefill_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int 
 /* Incremental metadata update after decoding (f1): with the metadata last
  * built at lengths prev_lens, rebuilds the rows of blocks
  * [prev_lens[b] / BS, ceil(seq_lens[b] / BS)) and zeroes the rows past the new
- * block count inside the used meta blocks; other rows are untouched.
+ * block count inside the meta blocks begun since prev_lens; other rows are
+ * untouched.
  * Prefill at prev_lens then this update equals prefill at seq_lens.
  * ORC_EINVAL when prev_lens[b] < 0 or > seq_lens[b]. */
 int orc_update_metadata(const void* k_cache, int kv_dt, int num_kv_blocks, int BS, int N, int D,

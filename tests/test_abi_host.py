@@ -30,9 +30,10 @@ def built_lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for f in ("qs_prefill_metadata", "qs_block_select_paged", "qs_probe_select",
-              "qs_sparse_decode_attn", "qs_sparse_decode_step", "qs_workspace_size",
-              "qs_read_status", "qs_status_string", "qs_version"):
+    for f in ("qs_prefill_metadata", "qs_update_metadata", "qs_block_select_paged",
+              "qs_probe_select", "qs_sparse_decode_attn", "qs_sparse_decode_step",
+              "qs_step_kernels", "qs_workspace_size", "qs_read_status", "qs_status_string",
+              "qs_version"):
         assert f in names
 
 

@@ -100,8 +100,8 @@ UPD_PREV, UPD_NEW = (0, 3, 13, 8), (0, 9, 21, 8)   # BS=4: empty, in-block, new 
 def test_metadata_update_rows_against_torch(dtype):
     """Rows of blocks [prev // BS, ceil(L / BS)) hold the amax/amin of the
     blocks' valid tokens at the new lengths, rows past the block count inside
-    the used meta blocks are zero, and every row below prev // BS keeps what
-    it held (planted values, not recomputed)."""
+    the meta blocks begun since prev are zero, and every other row keeps what
+    it held (planted values: neither recomputed nor re-zeroed)."""
     BS = 4
     k, bt, mbt, sl, M = ragged_case(dtype, B=4, BS=BS, seq_lens=UPD_NEW, MKBPR=6, MMBPR=2)
     N, D = k.shape[2], k.shape[3]
@@ -112,9 +112,10 @@ def test_metadata_update_rows_against_torch(dtype):
     mx_t, mn_t = from_bits(mx, dtype), from_bits(mn, dtype)
     for b, (P0, L) in enumerate(zip(UPD_PREV, UPD_NEW)):
         nb = (L + BS - 1) // BS
+        zero_from = (((P0 + BS - 1) // BS + BS - 1) // BS) * BS   # end of meta blocks in use
         for j in range(((nb + BS - 1) // BS) * BS):
             m, r = int(mbt[b, j // BS]), j % BS
-            if j < P0 // BS:
+            if j < P0 // BS or (nb <= j < zero_from):
                 assert torch.all(mx_t[m, r] == 3.0) and torch.all(mn_t[m, r] == 3.0), (b, j)
             elif j >= nb:
                 assert torch.all(mx_t[m, r] == 0) and torch.all(mn_t[m, r] == 0), (b, j)
