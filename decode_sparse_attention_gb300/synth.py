@@ -26,6 +26,8 @@ pages report):
   ragged           bf16, B=64, seq_len ~U[2048,131072] rounded to 128 and
                    clamped to >= k*BLOCK_SIZE, shuffled shared page pool,
                    MMBPR=8, k=32, sink+window on (t=0).
+Prefill queries for the importance producer (``prefill_queries``): one row
+per (position, query head) drawn like the decode query, over the same pages.
 """
 from __future__ import annotations
 
@@ -249,6 +251,19 @@ def make(w: Workload, seed: int = 0, device="cpu", seq_lens=None):
     out["P"] = P
     out["M"] = M
     return out
+
+
+def prefill_queries(w: Workload, S_max: int, seed: int = 0, device="cpu"):
+    """Query rows of a prefill of up to S_max tokens, [B, S_max, H, D], drawn
+    like the decode queries (U(-1,1) or N(0,1) per the workload) in the query
+    dtype; positions past a request's prefill length hold draws too and are
+    never read."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 7919)
+    shape = (w.B, S_max, w.H, w.D)
+    qf = _uniform(shape, gen, device) if w.q_dist == "uniform" else _normal(shape, gen, device)
+    return qf.to(TORCH_DTYPE[w.q_dtype])
 
 
 def softmax_scale(D):

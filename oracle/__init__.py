@@ -38,10 +38,12 @@ def lib():
         _lib.orc_sparse_attention.argtypes = [P, I, P, P, P, P, I, I, P, I, P, P, I, I, D, I, I,
                                               I, I, I, P, P]
         _lib.orc_quantize_query.argtypes = [P, I, I, P, P]
+        _lib.orc_prefill_importance.argtypes = [P, I, P, P, I, I, P, I, P, I, I, I, I, I, I, D,
+                                                I, P, P]
         for f in ("orc_prefill_metadata", "orc_update_metadata", "orc_group_mean_query",
                   "orc_quest_scores",
                   "orc_quest_select", "orc_forced_set", "orc_probe_select",
-                  "orc_sparse_attention", "orc_quantize_query"):
+                  "orc_sparse_attention", "orc_quantize_query", "orc_prefill_importance"):
             getattr(_lib, f).restype = ctypes.c_int
     return _lib
 
@@ -210,6 +212,29 @@ def sparse_attention(q, q_dt, k_cache, v_cache, kv_dt, block_tables, seq_lens, s
     return out, lse
 
 
-__all__ = ["F32", "BF16", "F16", "I8", "OracleError", "prefill_metadata", "group_mean_query",
-           "quest_scores", "quest_select", "forced_set", "quantize_query", "probe_select",
-           "sparse_attention", "lib"]
+def prefill_importance(q, q_dt, k_cache, kv_dt, block_tables, prefill_lens, N,
+                       softmax_scale=None, k_scale=None, first_query=0):
+    """f3 in double: q [B, S_max, H, D] (prefill queries), K through the
+    paged cache.  Returns (importance [B, S_max] float64, lse [B, H, S_max]
+    float64, NaN where not computed)."""
+    B, S_max, H, D = q.shape
+    P, BS, _, _ = k_cache.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / np.sqrt(D)
+    bt = _c(block_tables, np.int32)
+    q = _c(q, _elem_np(q_dt))
+    kc = _c(k_cache, _elem_np(kv_dt))
+    ks = None if k_scale is None else _c(k_scale, np.float32)
+    pl = _c(prefill_lens, np.int32)
+    imp = np.zeros((B, S_max), np.float64)
+    lse = np.full((B, H, S_max), np.nan)
+    rc = lib().orc_prefill_importance(_p(q), q_dt, _p(kc), _p(ks), kv_dt, P, _p(bt),
+                                      bt.shape[1], _p(pl), S_max, B, H, N, D, BS,
+                                      float(softmax_scale), int(first_query), _p(imp), _p(lse))
+    _check(rc, "prefill_importance")
+    return imp, lse
+
+
+__all__ = ["F32", "BF16", "F16", "I8", "OracleError", "prefill_metadata", "update_metadata",
+           "group_mean_query", "quest_scores", "quest_select", "forced_set", "quantize_query",
+           "probe_select", "sparse_attention", "prefill_importance", "lib"]

@@ -606,3 +606,85 @@ done:
     free(logit); free(vrow); free(srow); free(qd); free(qf); free(q8);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* f3: prefill importance (Kestrel 10-2 §1, signal 2: the attention each     */
+/* token received during an exact prefill, reduced per head and summed over  */
+/* the heads into prefill_importance[s]; §2, the decode call site: the sums  */
+/* are formed when the prefill ends)                                         */
+/* ------------------------------------------------------------------------ */
+
+int orc_prefill_importance(const void* q, int q_dt, const void* k_cache,
+                           const float* k_scale, int kv_dt, int num_kv_blocks,
+                           const int32_t* block_tables, int MKBPR,
+                           const int32_t* prefill_lens, int S_max, int B, int H, int N,
+                           int D, int BS, double softmax_scale, int first_query,
+                           double* importance, double* lse) {
+    if (B < 0 || N <= 0 || H % N != 0 || D <= 0 || BS <= 0 || S_max < 0) return ORC_EINVAL;
+    if (!is_float_dt(q_dt)) return ORC_EINVAL;
+    if (kv_dt == ORC_I8 ? !k_scale : !is_float_dt(kv_dt)) return ORC_EINVAL;
+    if (kv_dt != ORC_I8 && q_dt != kv_dt) return ORC_EINVAL;
+    const int G = H / N;
+    const size_t SD = (size_t)S_max * D;
+    /* keys of one (request, KV head) gathered in position order, the query
+     * row in double (or quantised), one row of logits, one head's masses */
+    double* kd = (double*)malloc(sizeof(double) * (SD + 1));
+    double* ks = (double*)malloc(sizeof(double) * ((size_t)S_max + 1));
+    double* logit = (double*)malloc(sizeof(double) * ((size_t)S_max + 1));
+    double* imp_head = (double*)malloc(sizeof(double) * ((size_t)S_max + 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+    float* qf = (float*)malloc(sizeof(float) * (size_t)D);
+    int8_t* q8 = (int8_t*)malloc((size_t)D);
+    int rc = ORC_OK;
+    if (!kd || !ks || !logit || !imp_head || !qd || !qf || !q8) { rc = ORC_EINVAL; goto done; }
+    for (int b = 0; b < B; b++) {
+        const int S = prefill_lens[b];
+        if (S < 0 || S > S_max || S > MKBPR * BS) { rc = ORC_EINVAL; goto done; }
+        double* imp = importance + (size_t)b * S_max;
+        for (int s = 0; s < S_max; s++) imp[s] = 0.0;
+        for (int h = 0; h < H; h++) {
+            const int n = h / G;
+            /* gather K of KV head n for positions 0..S-1 through the table */
+            for (int s = 0; s < S; s++) {
+                const int p = block_tables[(size_t)b * MKBPR + s / BS];
+                if (p < 0 || p >= num_kv_blocks) { rc = ORC_ERANGE; goto done; }
+                const size_t tok = ((size_t)p * BS + s % BS) * N + n;
+                for (int d = 0; d < D; d++)
+                    kd[(size_t)s * D + d] = kv_dt == ORC_I8
+                        ? (double)((const int8_t*)k_cache)[tok * D + d]
+                        : dec(k_cache, kv_dt, tok * D + d);
+                ks[s] = kv_dt == ORC_I8 ? (double)k_scale[tok] : 1.0;
+            }
+            for (int s = 0; s < S; s++) imp_head[s] = 0.0;
+            for (int i = first_query > 0 ? first_query : 0; i < S; i++) {
+                const size_t qoff = (((size_t)b * S_max + i) * H + h) * D;
+                double rowscale = 1.0;
+                for (int d = 0; d < D; d++) { qd[d] = dec(q, q_dt, qoff + d); qf[d] = (float)qd[d]; }
+                if (kv_dt == ORC_I8) {
+                    float s_q = 0.0f;
+                    orc_quantize_query(qf, ORC_F32, D, q8, &s_q);
+                    for (int d = 0; d < D; d++) qd[d] = (double)q8[d];
+                    rowscale = (double)s_q;
+                }
+                /* causal logits l_s, s <= i, then the row's log-sum-exp */
+                double m = -INFINITY;
+                for (int s = 0; s <= i; s++) {
+                    double dot = 0.0;
+                    for (int d = 0; d < D; d++) dot += qd[d] * kd[(size_t)s * D + d];
+                    logit[s] = softmax_scale * rowscale * ks[s] * dot;
+                    if (logit[s] > m) m = logit[s];
+                }
+                double z = 0.0;
+                for (int s = 0; s <= i; s++) z += exp(logit[s] - m);
+                const double row_lse = m + log(z);
+                if (lse) lse[((size_t)b * H + h) * S_max + i] = row_lse;
+                /* the mass this query gave each key */
+                for (int s = 0; s <= i; s++) imp_head[s] += exp(logit[s] - row_lse);
+            }
+            for (int s = 0; s < S; s++) imp[s] += imp_head[s];
+        }
+    }
+done:
+    free(kd); free(ks); free(logit); free(imp_head); free(qd); free(qf); free(q8);
+    return rc;
+}

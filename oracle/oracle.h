@@ -114,6 +114,28 @@ int orc_sparse_attention(const void* q, int q_dt, const void* k_cache,
  * Exposed so the tests can pin it. */
 int orc_quantize_query(const void* q, int q_dt, int D, int8_t* q8, float* s_q);
 
+/* Prefill importance (f3), double.  For request b with S = prefill_lens[b]
+ * prefill tokens, every query head h and every query position i < S attends
+ * causally to the keys s <= i of its KV head h / (H/N):
+ *   p[h][i][s] = exp(l_s - lse[h][i]),  l_s = softmax_scale * q[b][i][h] . K[b][s],
+ *   lse[h][i]  = log sum_{s<=i} exp(l_s);
+ * the per-head attention mass a token received, imp_head[h][s] = sum_{i>=s}
+ * p[h][i][s], is accumulated over the heads in ascending order into
+ * importance[b][s].  int8 KV: the query row is quantised as by
+ * orc_quantize_query and l_s = softmax_scale * s_q * k_scale[s] * (q8 . k8).
+ * q is [B, S_max, H, D]; K of position s sits in block_tables[b][s / BS],
+ * row s % BS.  Only query positions i >= first_query are summed (0: all), so
+ * importance[b][s] is exact for s >= first_query.  importance [B, S_max] is
+ * written for every s (0 for s >= S); lse [B, H, S_max] (optional) receives
+ * the rows first_query <= i < S.  ORC_EINVAL for S < 0 or
+ * S > min(S_max, MKBPR * BS); ORC_ERANGE for a bad table entry. */
+int orc_prefill_importance(const void* q, int q_dt, const void* k_cache,
+                           const float* k_scale, int kv_dt, int num_kv_blocks,
+                           const int32_t* block_tables, int MKBPR,
+                           const int32_t* prefill_lens, int S_max, int B, int H, int N,
+                           int D, int BS, double softmax_scale, int first_query,
+                           double* importance, double* lse);
+
 #ifdef __cplusplus
 }
 #endif

@@ -572,3 +572,142 @@ def test_probe_int8_score_is_scaled_integer_dot():
                 np.float32(int(np.dot(q8.astype(np.int64), k8[j, t, 0].astype(np.int64))))
                 for t in range(BS)]
         assert probe[0, 0, j] == max(dots)
+
+
+# --------------------------------------------------------------------------
+# f3 prefill importance
+# --------------------------------------------------------------------------
+
+def prefill_case(dtype, seed=0, B=2, H=4, N=2, D=16, BS=8, lens=(29, 0), S_max=32, zero_q=False):
+    """Paged prefill: K in a shuffled page pool, queries [B, S_max, H, D]."""
+    g = torch.Generator().manual_seed(seed)
+    MKBPR = (S_max + BS - 1) // BS
+    P = B * MKBPR + 2
+    if dtype == torch.int8:
+        kc = torch.randint(-127, 128, (P, BS, N, D), generator=g).to(torch.int8)
+        ks = torch.rand((P, BS, N), generator=g) / 127 + 0.001
+        q = torch.rand((B, S_max, H, D), generator=g) * 4 - 2
+    else:
+        kc = torch.randn((P, BS, N, D), generator=g).to(dtype)
+        ks = None
+        q = (torch.rand((B, S_max, H, D), generator=g) * 4 - 2).to(dtype)
+    if zero_q:
+        q = torch.zeros_like(q)
+    bt = torch.randperm(P, generator=g)[:B * MKBPR].reshape(B, MKBPR).to(torch.int32)
+    return q, kc, ks, bt, np.array(lens, np.int32)
+
+
+def gathered_keys(kc, ks, bt, b, S, n, BS):
+    """K of KV head n, positions 0..S-1, in position order (fp64; int8 keys
+    dequantised with their scales)."""
+    rows = [kc[int(bt[b, s // BS]), s % BS, n].double() for s in range(S)]
+    K = torch.stack(rows) if rows else torch.zeros((0, kc.shape[-1]), dtype=torch.float64)
+    if ks is not None and S:
+        K = K * torch.stack([ks[int(bt[b, s // BS]), s % BS, n].double() for s in range(S)])[:, None]
+    return K
+
+
+def sdpa_importance(qd, Kh, scale):
+    """Column sums of the causal attention matrix through torch SDPA: with the
+    values one-hot (V = I), output row i is row i of the probability matrix,
+    so summing the outputs over positions and heads gives the mass each key
+    received.  qd [H, S, D], Kh [H, S, D] fp64."""
+    H, S, _ = qd.shape
+    V = torch.eye(S, dtype=torch.float64).expand(H, S, S)
+    P = torch.nn.functional.scaled_dot_product_attention(qd[None], Kh[None], V[None],
+                                                         is_causal=True, scale=scale)[0]
+    return P.sum(dim=(0, 1))
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16, torch.float16])
+def test_prefill_importance_equals_sdpa_column_sums(dtype):
+    BS, H, N, D = 8, 4, 2, 16
+    q, kc, _, bt, lens = prefill_case(dtype, seed=3, H=H, N=N, D=D, BS=BS, lens=(29, 17))
+    scale = 1 / np.sqrt(D)
+    imp, lse = oracle.prefill_importance(to_np(q), odt(q), to_np(kc), odt(kc), to_np(bt), lens, N)
+    G = H // N
+    for b, S in enumerate(lens.tolist()):
+        qd = q[b, :S].double().permute(1, 0, 2)                       # [H, S, D]
+        Kh = torch.stack([gathered_keys(kc, None, bt, b, S, h // G, BS) for h in range(H)])
+        ref = sdpa_importance(qd, Kh, scale)
+        assert np.allclose(imp[b, :S], ref.numpy(), rtol=1e-12, atol=1e-12)
+        assert np.all(imp[b, S:] == 0)
+        # lse of each row: log-sum-exp of its causal logits (library routine)
+        logits = torch.einsum("hid,hsd->his", qd, Kh) * scale
+        mask = torch.ones(S, S, dtype=torch.bool).tril()
+        ref_lse = torch.logsumexp(logits.masked_fill(~mask, -np.inf), dim=-1)
+        assert np.allclose(lse[b, :, :S], ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_importance_uniform_closed_form():
+    """q = 0: every row is uniform over its i+1 keys, so lse = log(i+1) and
+    importance[s] = H * sum_{i=s}^{S-1} 1/(i+1)."""
+    BS, H, N = 8, 6, 3
+    q, kc, _, bt, lens = prefill_case(torch.float32, seed=1, H=H, N=N, BS=BS, lens=(31, 5),
+                                      zero_q=True)
+    imp, lse = oracle.prefill_importance(to_np(q), odt(q), to_np(kc), odt(kc), to_np(bt), lens, N)
+    for b, S in enumerate(lens.tolist()):
+        harm = np.array([sum(1.0 / (i + 1) for i in range(s, S)) for s in range(S)])
+        assert np.allclose(imp[b, :S], H * harm, rtol=1e-13, atol=0)
+        assert np.allclose(lse[b, :, :S], np.log(np.arange(1, S + 1))[None], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_prefill_importance_mass_conservation(seed):
+    """Every query row sums to one: sum_s importance = H * S; importance >= 0;
+    the last token is seen only by the last query."""
+    BS, H, N, D = 4, 8, 2, 8
+    q, kc, _, bt, lens = prefill_case(torch.float32, seed=seed, H=H, N=N, D=D, BS=BS,
+                                      lens=(23, 1), S_max=24)
+    imp, lse = oracle.prefill_importance(to_np(q), odt(q), to_np(kc), odt(kc), to_np(bt), lens, N)
+    for b, S in enumerate(lens.tolist()):
+        assert np.isclose(imp[b].sum(), H * S, rtol=1e-13)
+        assert np.all(imp[b, :S] > 0)
+    # row 0 of every head attends only to key 0: lse = its own logit
+    G = H // N
+    K0 = kc[int(bt[0, 0]), 0].double()
+    for h in range(H):
+        l00 = float(q[0, 0, h].double() @ K0[h // G]) / np.sqrt(D)
+        assert np.isclose(lse[0, h, 0], l00, rtol=0, atol=1e-13)
+
+
+def test_prefill_importance_int8_equals_dequantised_sdpa():
+    """int8 keys: the query row quantised as for decode, logits from the exact
+    integer dot times s_q * s_k; equal to SDPA on the dequantised operands."""
+    BS, H, N, D = 8, 4, 2, 16
+    q, kc, ks, bt, lens = prefill_case(torch.int8, seed=5, H=H, N=N, D=D, BS=BS, lens=(21, 30))
+    imp, _ = oracle.prefill_importance(q.numpy(), oracle.F32, kc.numpy(), oracle.I8, to_np(bt),
+                                       lens, N, k_scale=ks.numpy())
+    G = H // N
+    for b, S in enumerate(lens.tolist()):
+        qd = torch.zeros((H, S, D), dtype=torch.float64)
+        for h in range(H):
+            for i in range(S):
+                q8, s_q = oracle.quantize_query(q[b, i, h].numpy())
+                qd[h, i] = torch.from_numpy(q8.astype(np.float64)) * s_q
+        Kh = torch.stack([gathered_keys(kc, ks, bt, b, S, h // G, BS) for h in range(H)])
+        ref = sdpa_importance(qd, Kh, 1 / np.sqrt(D))
+        assert np.allclose(imp[b, :S], ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_importance_first_query_and_errors():
+    """Summing only the queries from position f on leaves importance[s >= f]
+    unchanged (a key is seen only by later queries); bad lengths and table
+    entries are rejected."""
+    BS, H, N, D = 8, 4, 2, 16
+    q, kc, _, bt, lens = prefill_case(torch.float32, seed=7, H=H, N=N, D=D, BS=BS, lens=(30, 19))
+    full, lse_full = oracle.prefill_importance(to_np(q), odt(q), to_np(kc), odt(kc), to_np(bt),
+                                               lens, N)
+    f = 12
+    part, lse_part = oracle.prefill_importance(to_np(q), odt(q), to_np(kc), odt(kc), to_np(bt),
+                                               lens, N, first_query=f)
+    assert np.array_equal(part[:, f:], full[:, f:])
+    assert np.array_equal(lse_part[:, :, f:], lse_full[:, :, f:], equal_nan=True)
+    assert np.all(np.isnan(lse_part[:, :, :f]))
+    with pytest.raises(oracle.OracleError):
+        oracle.prefill_importance(to_np(q), odt(q), to_np(kc), odt(kc), to_np(bt),
+                                  np.array([33, 0], np.int32), N)
+    bad = to_np(bt).copy()
+    bad[0, 1] = kc.shape[0]
+    with pytest.raises(oracle.OracleError):
+        oracle.prefill_importance(to_np(q), odt(q), to_np(kc), odt(kc), bad, lens, N)
