@@ -15,6 +15,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libquestsparse.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = ["qs_api.cu", "qs_metadata.cu", "qs_select.cu", "qs_probe.cu", "qs_attention.cu",
+           "qs_importance.cu",
            "qs_attention_noalloc.cu", "qs_step_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -79,11 +79,16 @@ def lib():
             L.qs_sparse_decode_attn.argtypes = [P, I32, P, P, P, P, I32, I32, P, I32, P, P, I32,
                                                 I32, F, I32, I32, I32, I32, I32, P, P, P, SZ, P,
                                                 P]
+            L.qs_prefill_importance_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32,
+                                                               ctypes.POINTER(SZ)]
+            L.qs_prefill_importance.argtypes = [P, I32, P, P, I32, I32, P, I32, P, I32, I32, I32,
+                                                I32, I32, I32, F, P, P, P, SZ, P, P]
             L.qs_sparse_decode_step.argtypes = [ctypes.POINTER(StepParams), P]
             L.qs_step_kernels.argtypes = [ctypes.POINTER(StepParams), P]
             for f in ("qs_read_status", "qs_workspace_size", "qs_prefill_metadata",
                       "qs_block_select_paged", "qs_probe_select", "qs_sparse_decode_attn",
-                      "qs_sparse_decode_step"):
+                      "qs_sparse_decode_step", "qs_update_metadata", "qs_step_kernels",
+                      "qs_prefill_importance_workspace_size", "qs_prefill_importance"):
                 getattr(L, f).restype = I32
             _lib = L
     return _lib
@@ -311,6 +316,50 @@ def probe_select(q, k_cache, block_tables, seq_lens, k, n_probe=8, importance=No
                                _ptr(status_word(q.device)), _stream(q.device))
     _check(rc, "qs_probe_select")
     return selected
+
+
+def prefill_importance_workspace_size(B, H, N, D, S_max, kv_dtype):
+    n = SZ(0)
+    _check(lib().qs_prefill_importance_workspace_size(B, H, N, D, S_max, kv_dtype,
+                                                      ctypes.byref(n)),
+           "qs_prefill_importance_workspace_size")
+    return n.value
+
+
+def prefill_importance(q, k_cache, block_tables, prefill_lens, softmax_scale=None, k_scale=None,
+                       importance=None, lse=None):
+    """Prefill importance: the attention each prefill token received, summed
+    over query heads and later query positions (causal, exact).
+
+    q: [B, S_max, H, D] prefill query rows; K through block_tables into
+    k_cache [P, BS, N, D].  Returns importance [B, S_max] fp32 (the layout
+    probe_select takes); fills lse [B, H, S_max] when given."""
+    _req(q, "q", dim=4)
+    B, S_max, H, D = q.shape
+    _req(k_cache, "k_cache", dim=4)
+    P_, BS, N, D2 = k_cache.shape
+    if D2 != D:
+        raise QuestSparseError("head dim mismatch")
+    _req(block_tables, "block_tables", torch.int32, 2)
+    _req(prefill_lens, "prefill_lens", torch.int32, 1)
+    if k_scale is not None:
+        _req(k_scale, "k_scale", torch.float32, 3)
+    if importance is None:
+        importance = torch.empty((B, S_max), dtype=torch.float32, device=q.device)
+    _req(importance, "importance", torch.float32, 2)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, 3)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    nbytes = prefill_importance_workspace_size(B, H, N, D, S_max, _dt(k_cache))
+    ws = workspace(nbytes, q.device, ("importance", B, H, N, D, S_max))
+    rc = lib().qs_prefill_importance(_ptr(q), _dt(q), _ptr(k_cache), _ptr(k_scale), _dt(k_cache),
+                                     P_, _ptr(block_tables), block_tables.shape[1],
+                                     _ptr(prefill_lens), S_max, B, H, N, D, BS,
+                                     float(softmax_scale), _ptr(importance), _ptr(lse), _ptr(ws),
+                                     ws.numel(), _ptr(status_word(q.device)), _stream(q.device))
+    _check(rc, "qs_prefill_importance")
+    return importance
 
 
 def sparse_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, selected, softmax_scale=None,

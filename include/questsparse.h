@@ -302,6 +302,43 @@ qs_status qs_sparse_decode_step(const qs_step_params* params, qs_stream_t stream
  * QS_EWORKSPACE when the workspace is too small to hold the selector part. */
 qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
 
+/*
+ * Prefill importance producer (Kestrel-LLM 10-2, section 1, signal 2, and the
+ * decode call site in section 2: the attention each prefill token received,
+ * reduced per head and summed over the heads into prefill_importance[s] when
+ * the prefill ends).  For request b with S = prefill_lens[b] tokens, query
+ * head h (KV head n = h / (H/N)) and query position i < S, over the keys
+ * s <= i of the request (causal, exact):
+ *   l_s = softmax_scale * q[b][i][h] . K[s]   (int8 caches: softmax_scale *
+ *         s_q*s_k * int_dot, the query row quantised per (i, h) exactly as the
+ *         decode calls do: s_q = max|q|/127, q8 = rint(q/s_q)),
+ *   lse = log sum_{s<=i} exp(l_s),   p_s = exp(l_s - lse),
+ *   importance[b][s] = sum over h and i >= s of p_s   (fp32, [B, S_max];
+ *         0 for s >= S; sum_s importance[b][s] = H * S).
+ * q: [B, S_max, H, D] prefill query rows (fp32, bf16 or fp16; equal to
+ * kv_dtype unless kv_dtype is int8).  K of position s: row s % BS of KV block
+ * block_tables[b][s / BS] of k_cache [num_kv_blocks, BS, N, D] (k_scale
+ * [num_kv_blocks, BS, N] fp32 for int8).  lse_opt: NULL or [B, H, S_max] fp32,
+ * rows i < S receive lse (natural log).  D in {64, 128}; H/N a power of two
+ * <= 64.  Computed in fp32 on the CUDA cores in two passes (row log-sum-exp,
+ * then column mass, each recomputing the logits; summation order is the
+ * kernel's).  workspace: qs_prefill_importance_workspace_size bytes, no
+ * initial contents needed.  Device errors: a table entry outside
+ * [0, num_kv_blocks) -> QS_DEV_EBLOCK_TABLE; S < 0 or S > min(S_max,
+ * MKBPR*BS) -> QS_DEV_ESEQ_LEN, and that request's importance is left zero.
+ */
+qs_status qs_prefill_importance_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D,
+                                               int32_t S_max, qs_dtype kv_dtype,
+                                               size_t* bytes);
+qs_status qs_prefill_importance(const void* q, qs_dtype q_dtype, const void* k_cache,
+                                const float* k_scale, qs_dtype kv_dtype,
+                                int32_t num_kv_blocks, const int32_t* block_tables,
+                                int32_t MKBPR, const int32_t* prefill_lens, int32_t S_max,
+                                int32_t B, int32_t H, int32_t N, int32_t D, int32_t BS,
+                                float softmax_scale, float* importance, float* lse_opt,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                qs_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

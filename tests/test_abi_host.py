@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     for f in ("qs_prefill_metadata", "qs_update_metadata", "qs_block_select_paged",
               "qs_probe_select", "qs_sparse_decode_attn", "qs_sparse_decode_step",
               "qs_step_kernels", "qs_workspace_size", "qs_read_status", "qs_status_string",
-              "qs_version"):
+              "qs_version", "qs_prefill_importance", "qs_prefill_importance_workspace_size"):
         assert f in names
 
 
@@ -61,6 +61,20 @@ def test_workspace_size_without_gpu(built_lib):
     assert s >= n + a
     with pytest.raises(qs.QuestSparseError):
         qs.workspace_size(qs.OP_SPARSE_ATTN, 2, 32, 8, 128, 128, 8, 128, 5)   # sel_heads
+
+
+def test_prefill_importance_workspace_without_gpu(built_lib):
+    """Row log-sum-exps (B*H*S_max fp32) plus per-part column sums; int8
+    caches add the quantised query rows and their scales."""
+    from decode_sparse_attention_gb300 import questsparse as qs
+    f = qs.prefill_importance_workspace_size(1, 16, 8, 128, 4096, qs.F32)
+    assert f >= 16 * 4096 * 4 + 8 * 4096 * 4
+    i8 = qs.prefill_importance_workspace_size(1, 16, 8, 128, 4096, qs.I8)
+    assert i8 >= f + 4096 * 16 * 128 + 4096 * 16 * 4
+    with pytest.raises(qs.QuestSparseError):
+        qs.prefill_importance_workspace_size(1, 24, 8, 128, 4096, qs.F32)   # H/N = 3
+    with pytest.raises(qs.QuestSparseError):
+        qs.prefill_importance_workspace_size(1, 16, 8, 96, 4096, qs.F32)   # D
 
 
 def test_binding_rejects_host_tensors(built_lib):
