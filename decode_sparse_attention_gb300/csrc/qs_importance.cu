@@ -21,6 +21,7 @@
 // The inputs are fp32 on the pages' engine; tensor cores would round them to
 // tf32/bf16 first, so the contraction stays on the FP32 pipes.
 #include <cmath>
+#include <type_traits>
 
 #include "qs_common.cuh"
 
@@ -48,6 +49,8 @@ struct Args {
     float* importance;        // [B, S_max]
     int32_t* status;
     int P, MKBPR, S_max, B, H, N, G, BS;
+    int g_shift;              // log2 G
+    int bs_shift;             // log2 BS, or -1 when BS is not a power of two
     int parts, part_tiles;    // pass 2 split of the query tiles
     float scale_log2;         // softmax_scale * log2(e)
 };
@@ -211,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_pass_kernel(const Args
         }
         __syncthreads();
     }
+    auto blk_of = [&](int s) { return a.bs_shift >= 0 ? s >> a.bs_shift : s / a.BS; };
     auto entry = [&](int j) -> int {
         if constexpr (!kCols) {
             if (staged) return s_tab[j];
@@ -226,7 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1) importance_pass_kernel(const Args
         return a.q + ((static_cast<size_t>(b) * a.S_max + i) * a.H + h0 + g) * q_row_bytes;
     };
     auto k_tok = [&](int e, int s) {
-        return (static_cast<size_t>(e) * a.BS + s % a.BS) * a.N + n;
+        const int row = a.bs_shift >= 0 ? (s & (a.BS - 1)) : s % a.BS;
+        return (static_cast<size_t>(e) * a.BS + row) * a.N + n;
     };
 
     // resident rows (fp32) and their position / factor
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_pass_kernel(const Args
         } else {
             const int s = base + r;
             if (s < S) {
-                const int e = entry(s / a.BS);
+                const int e = entry(blk_of(s));
                 if (e >= 0) src = a.k + k_tok(e, s) * k_row_bytes;
             }
         }
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_pass_kernel(const Args
         } else {
             const int s = base + r;
             if (s < S) {
-                const int e = entry(s / a.BS);
+                const int e = entry(blk_of(s));
                 if (e >= 0) {
                     pos = s;
                     if constexpr (kInt8) fac = a.k_scale[k_tok(e, s)];
@@ -274,52 +279,50 @@ __global__ void __launch_bounds__(kThreads, 1) importance_pass_kernel(const Args
         s_rfac[r] = fac;
     }
 
-    // streamed tile t -> ring slot buf (fp32 rows directly, others raw)
+    // streamed tile t -> ring slot buf: 4 threads per row, each copying every
+    // 4th 16-byte chunk of it (fp32 rows straight into the ring, others raw)
     auto issue = [&](int t, int buf) {
-        float* dstf = s_str + buf * kStr * pitch;
-        uint8_t* dstr = s_stg + buf * kStr * L::raw_row;
-        for (int c = tid; c < kStr * SCPR; c += kThreads) {
-            const int r = c / SCPR, ch = c - r * SCPR;
-            const uint8_t* src = nullptr;
-            if constexpr (!kCols) {
-                const int s = t * kStr + r;
-                if (s < S) {
-                    const int e = entry(s / a.BS);
-                    if (e >= 0) src = a.k + k_tok(e, s) * k_row_bytes;
+        const int r = tid >> 2, c0 = tid & 3;
+        const uint8_t* src = nullptr;
+        int pos = -1;
+        size_t tok = 0;
+        if constexpr (!kCols) {
+            const int s = t * kStr + r;
+            if (s < S) {
+                const int e = entry(blk_of(s));
+                if (e >= 0) {
+                    tok = k_tok(e, s);
+                    src = a.k + tok * k_row_bytes;
+                    pos = s;
                 }
-            } else {
-                const int i = t * TQs + r / G;
-                if (i < S) src = q_src(i, r % G);
             }
-            void* dst;
-            if constexpr (ST == Dt::F32) dst = dstf + r * pitch + ch * 4;
-            else dst = dstr + r * L::raw_row + ch * 16;
-            if (src) cpa16(smem_addr(dst), src + ch * 16);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            const int i = t * TQs + (r >> a.g_shift);
+            if (i < S) {
+                src = q_src(i, r & (G - 1));
+                pos = i;
+            }
         }
-        if (tid < kStr) {
-            const int r = tid;
-            int pos = -1;
-            if constexpr (!kCols) {
-                const int s = t * kStr + r;
-                if (s < S) {
-                    const int e = entry(s / a.BS);
-                    if (e >= 0) {
-                        pos = s;
-                        if constexpr (kInt8)
-                            cpa4(smem_addr(s_sfac + buf * kStr + r), a.k_scale + k_tok(e, s));
-                    }
-                }
-            } else {
-                const int i = t * TQs + r / G;
-                if (i < S) {
-                    const int g = r % G;
-                    pos = i;
+        uint8_t* dst = ST == Dt::F32
+                           ? reinterpret_cast<uint8_t*>(s_str + (buf * kStr + r) * pitch)
+                           : s_stg + (buf * kStr + r) * L::raw_row;
+#pragma unroll
+        for (int j = 0; j < SCPR / 4; ++j) {
+            const int ch = c0 + 4 * j;
+            if (src) cpa16(smem_addr(dst + ch * 16), src + ch * 16);
+            else *reinterpret_cast<uint4*>(dst + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (c0 == 0) {
+            if (pos >= 0) {
+                if constexpr (!kCols) {
+                    if constexpr (kInt8) cpa4(smem_addr(s_sfac + buf * kStr + r), a.k_scale + tok);
+                } else {
+                    const int g = r & (G - 1);
                     cpa4(smem_addr(s_slse + buf * kStr + r),
-                         a.lse2 + bn_rows * a.S_max * G + static_cast<size_t>(i) * G + g);
+                         a.lse2 + bn_rows * a.S_max * G + static_cast<size_t>(pos) * G + g);
                     if constexpr (kInt8)
                         cpa4(smem_addr(s_sfac + buf * kStr + r),
-                             a.s_q + (static_cast<size_t>(b) * a.S_max + i) * a.H + h0 + g);
+                             a.s_q + (static_cast<size_t>(b) * a.S_max + pos) * a.H + h0 + g);
                 }
             }
             s_spos[buf * kStr + r] = pos;
@@ -354,14 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1) importance_pass_kernel(const Args
             __syncthreads();
         }
 
-        // 8 x 4 logits: even channels in the low lane, odd in the high lane
+        // 8 x 4 dot products: even channels in the low lane, odd in the high
+        // lane; all first halves of a 4-channel step before the second halves
         const float* Sm = s_str + buf * kStr * pitch;
         unsigned long long acc[8][4];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc[u][v] = 0ull;
-#pragma unroll 2
+#pragma unroll 4
         for (int d = 0; d < D; d += 4) {
             ulonglong2 rv[8], sv[4];
 #pragma unroll
@@ -373,61 +377,85 @@ __global__ void __launch_bounds__(kThreads, 1) importance_pass_kernel(const Args
 #pragma unroll
             for (int u = 0; u < 8; ++u)
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    acc[u][v] = fma2(rv[u].x, sv[v].x, acc[u][v]);
-                    acc[u][v] = fma2(rv[u].y, sv[v].y, acc[u][v]);
-                }
+                for (int v = 0; v < 4; ++v) acc[u][v] = fma2(rv[u].x, sv[v].x, acc[u][v]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) acc[u][v] = fma2(rv[u].y, sv[v].y, acc[u][v]);
         }
 
+        // Logit arithmetic, identical in both passes: a = dot, then
+        //   fp caches:   2^(fma(a, qf, -ref))            (qf = scale * log2 e > 0)
+        //   int8 caches: 2^((a * qf) * kf - ref)         (qf with s_q, kf = s_k)
+        // A tile wholly inside the causal triangle and the lengths skips the masks.
         const int* spos = s_spos + buf * kStr;
-        if constexpr (!kCols) {
-            // online row max / sum over this thread's 4 keys
+        auto epilogue = [&](auto masked_tag) {
+            constexpr bool kMasked = decltype(masked_tag)::value;
+            if constexpr (!kCols) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int ipos = s_rpos[rg + 16 * u];
-                if (ipos < 0) continue;
-                const float qf = s_rfac[rg + 16 * u];
-                float lv[4];
-                float tmax = -INFINITY;
+                for (int u = 0; u < 8; ++u) {
+                    const int ipos = s_rpos[rg + 16 * u];
+                    if (kMasked && ipos < 0) continue;
+                    const float qf = s_rfac[rg + 16 * u];
+                    float x[4];
+                    bool ok[4];
+                    float tmax = -INFINITY;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int sr = sg + 16 * v;
+                        const float2 f = unpack2(acc[u][v]);
+                        x[v] = __fadd_rn(f.x, f.y);
+                        if constexpr (kInt8) x[v] = __fmul_rn(__fmul_rn(x[v], qf), s_sfac[buf * kStr + sr]);
+                        ok[v] = true;
+                        if constexpr (kMasked) {
+                            const int kp = spos[sr];
+                            ok[v] = kp >= 0 && kp <= ipos;
+                        }
+                        if (ok[v]) tmax = fmaxf(tmax, x[v]);
+                    }
+                    if (kMasked && tmax == -INFINITY) continue;
+                    if constexpr (!kInt8) tmax = __fmul_rn(tmax, qf);
+                    if (tmax > st_a[u]) {
+                        st_b[u] *= exp2_approx(st_a[u] - tmax);
+                        st_a[u] = tmax;
+                    }
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (!ok[v]) continue;
+                        if constexpr (kInt8) st_b[u] += exp2_approx(x[v] - st_a[u]);
+                        else st_b[u] += exp2_approx(fmaf(x[v], qf, -st_a[u]));
+                    }
+                }
+            } else {
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                     const int sr = sg + 16 * v;
-                    const float2 f = unpack2(acc[u][v]);
-                    float l = __fmul_rn(__fadd_rn(f.x, f.y), qf);
-                    if constexpr (kInt8) l = __fmul_rn(l, s_sfac[buf * kStr + sr]);
-                    const int kp = spos[sr];
-                    lv[v] = (kp >= 0 && kp <= ipos) ? l : -INFINITY;
-                    tmax = fmaxf(tmax, lv[v]);
-                }
-                if (tmax == -INFINITY) continue;
-                if (tmax > st_a[u]) {
-                    st_b[u] *= exp2_approx(st_a[u] - tmax);
-                    st_a[u] = tmax;
-                }
+                    const int ipos = spos[sr];
+                    if (kMasked && ipos < 0) continue;
+                    const float lse = s_slse[buf * kStr + sr];
+                    float qf = a.scale_log2;
+                    if constexpr (kInt8) qf = __fmul_rn(s_sfac[buf * kStr + sr], a.scale_log2);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) st_b[u] += exp2_approx(lv[v] - st_a[u]);
-            }
-        } else {
-            // probabilities with the rows' log-sum-exp, summed per key
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int sr = sg + 16 * v;
-                const int ipos = spos[sr];
-                if (ipos < 0) continue;
-                const float lse = s_slse[buf * kStr + sr];
-                float qf = a.scale_log2;
-                if constexpr (kInt8) qf = __fmul_rn(s_sfac[buf * kStr + sr], a.scale_log2);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int kp = s_rpos[rg + 16 * u];
-                    if (kp < 0 || kp > ipos) continue;
-                    const float2 f = unpack2(acc[u][v]);
-                    float l = __fmul_rn(__fadd_rn(f.x, f.y), qf);
-                    if constexpr (kInt8) l = __fmul_rn(l, s_rfac[rg + 16 * u]);
-                    st_a[u] += exp2_approx(l - lse);
+                    for (int u = 0; u < 8; ++u) {
+                        if constexpr (kMasked) {
+                            const int kp = s_rpos[rg + 16 * u];
+                            if (kp < 0 || kp > ipos) continue;
+                        }
+                        const float2 f = unpack2(acc[u][v]);
+                        const float x = __fadd_rn(f.x, f.y);
+                        if constexpr (kInt8)
+                            st_a[u] += exp2_approx(__fmul_rn(__fmul_rn(x, qf), s_rfac[rg + 16 * u]) - lse);
+                        else
+                            st_a[u] += exp2_approx(fmaf(x, qf, -lse));
+                    }
                 }
             }
-        }
+        };
+        bool interior;
+        if constexpr (!kCols) interior = t * kStr + kStr - 1 <= base && base + kRes / G - 1 < S;
+        else interior = base + kRes - 1 <= t * TQs && t * TQs + TQs - 1 < S;
+        if (interior) epilogue(std::false_type{});
+        else epilogue(std::true_type{});
     }
 
     // combine the 16 streamed groups of every resident row (scratch: ring)
@@ -620,7 +648,8 @@ extern "C" qs_status qs_prefill_importance(const void* q, qs_dtype q_dtype, cons
                                            qs_stream_t stream) {
     const qs_status rc = check_dims(B, H, N, D, S_max);
     if (rc != QS_OK) return rc;
-    if (BS <= 0 || MKBPR < 0 || num_kv_blocks < 0 || !std::isfinite(softmax_scale))
+    if (BS <= 0 || MKBPR < 0 || num_kv_blocks < 0 || !std::isfinite(softmax_scale) ||
+        !(softmax_scale > 0.f))
         return QS_EINVAL;
     if (B == 0 || S_max == 0) return QS_OK;
     const bool int8 = kv_dtype == QS_I8;
@@ -659,7 +688,9 @@ extern "C" qs_status qs_prefill_importance(const void* q, qs_dtype q_dtype, cons
     a.H = H;
     a.N = N;
     a.G = H / N;
+    a.g_shift = __builtin_ctz(static_cast<unsigned>(a.G));
     a.BS = BS;
+    a.bs_shift = (BS & (BS - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(BS)) : -1;
     a.parts = w.parts;
     a.part_tiles = w.part_tiles;
     a.scale_log2 = softmax_scale * kLog2e;

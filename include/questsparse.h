@@ -4,9 +4,9 @@
  *
  * Operations and where they are defined:
  *   qs_prefill_metadata    CANN ops-transformer select_attention_operators page
- *   qs_update_metadata     the same page (metadata refreshed while decoding)
  *                          (Quest on Ascend 910B), section 'quest_prefill_metadata:
  *                          metadata construction'.
+ *   qs_update_metadata     the same page (metadata refreshed while decoding).
  *   qs_block_select_paged  same page, section 'quest_block_select_paged: decode-time
  *                          top-k prediction' (steps 1, 2.1-2.3) and the three
  *                          interfaces ('_in_out' / '_in_out_w': the sink + window
@@ -19,6 +19,9 @@
  *                          with the in-sequence -> physical mapping through
  *                          block_tables from the CANN page's top-k section.
  *   qs_sparse_decode_step  select (either mode) followed by the attention.
+ *   qs_prefill_importance  Kestrel-LLM 10-2 section 1, signal 2 (the attention each
+ *                          prefill token received, per head, summed over heads),
+ *                          the input qs_probe_select's importance budget reads.
  *
  * Conventions shared by every call:
  *  - All tensor arguments are DEVICE pointers to contiguous row-major memory
@@ -320,7 +323,7 @@ qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
  * block_tables[b][s / BS] of k_cache [num_kv_blocks, BS, N, D] (k_scale
  * [num_kv_blocks, BS, N] fp32 for int8).  lse_opt: NULL or [B, H, S_max] fp32,
  * rows i < S receive lse (natural log).  D in {64, 128}; H/N a power of two
- * <= 64.  Computed in fp32 on the CUDA cores in two passes (row log-sum-exp,
+ * <= 64; softmax_scale > 0.  Computed in fp32 on the CUDA cores in two passes (row log-sum-exp,
  * then column mass, each recomputing the logits; summation order is the
  * kernel's).  workspace: qs_prefill_importance_workspace_size bytes, no
  * initial contents needed.  Device errors: a table entry outside
