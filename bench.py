@@ -296,6 +296,52 @@ def metadata_update(w, x, dev, flush, sink, reps=5):
     return statistics.median(times), nbytes
 
 
+def prefill_importance_timing(dev, clocks, reps=5):
+    """The prefill importance producer on the probe_importance shape (B=1,
+    S=4096, H=16, N=8, D=128, fp32 cache): median of `reps` calls timed with
+    CUDA events after two warm-up calls.  Its inputs (48 MB) are read from L2
+    after the first tile; the kernels are bound by the FP32 pipes, so the
+    roofline is the FP32 FMA rate: SMs x 128 lanes x 2 flop x max SM clock.
+    Algorithmic flops count one logit (2*D) per causal (query row, key) pair;
+    the kernels form every logit twice (row pass, column pass)."""
+    from decode_sparse_attention_gb300 import questsparse as qs
+    from decode_sparse_attention_gb300 import synth
+    w = synth.WORKLOADS["probe_importance"]
+    x = synth.make(w, seed=0, device=dev)
+    S_max = x["MKBPR"] * w.BS
+    q = synth.prefill_queries(w, S_max, seed=0, device=dev)
+    args = (q, x["k_cache"], x["block_tables"], x["seq_lens"])
+    for _ in range(2):
+        qs.prefill_importance(*args)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        qs.prefill_importance(*args)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(1000.0 * e0.elapsed_time(e1))
+    us = statistics.median(times)
+    pairs = sum(int(S) * (int(S) + 1) // 2 for S in x["seq_lens"].cpu().tolist())
+    alg = 2.0 * w.D * w.H * pairs
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_max_mhz") or 2070.0
+    peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+    return {
+        "kernels": "importance_pass_kernel (rows, columns) + importance_sum_kernel",
+        "workload": "probe_importance prefill: B=1 S=4096 H=16 N=8 D=128 BLOCK_SIZE=32 fp32",
+        "us": round(us, 1),
+        "bound": "alu",
+        "algorithmic_tflops": round(alg / (us * 1e-6) / 1e12, 2),
+        "executed_tflops": round(2 * alg / (us * 1e-6) / 1e12, 2),
+        "peak_tflops": round(peak, 1),
+        "peak_kind": "derived: %d SMs x 128 FP32 lanes x 2 flop x %.0f MHz" % (sms, mhz),
+        "frac_executed": round(2 * alg / (us * 1e-6) / 1e12 / peak, 4),
+        "status": qs.read_status(dev),
+    }
+
+
 def flush_l2(flush, sink):
     """Evict the L2: write a buffer twice the L2 size, then read it back, so
     the next kernel starts with none of its inputs cached and no dirty lines
@@ -539,6 +585,8 @@ def run_ours(args, w):
                     for l in x0["seq_lens"].cpu().numpy())
         mbytes = mrows * w.N * w.D * elem_bytes(x0["k_cache"].dtype) * 2
         res["metadata_prefill_gbs"] = round((kbytes + mbytes) / (meta_ms * 1e-3) / 1e9, 1)
+    if rank == 0 and not args.no_importance:
+        res["prefill_importance"] = prefill_importance_timing(dev, clocks)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, x0, args.cpu_seconds)
     if ws_ > 1:
@@ -676,6 +724,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-importance", action="store_true",
+                    help="skip timing the prefill importance producer")
     ap.add_argument("--max-sets", type=int, default=24,
                     help="most input sets to rotate through; workloads needing more (tiny "
                          "steps) are timed with an L2 flush between steps instead")
