@@ -568,14 +568,14 @@ struct WsPlan {
 };
 
 // Pass 2 splits each key tile's query range into up to kMaxParts parts of
-// about 32 streamed tiles, so that the keys near the start of a long prefill
+// about 16 streamed tiles, so that the keys near the start of a long prefill
 // (seen by every query) do not leave one CTA working long after the rest.
 WsPlan plan_ws(long long B, long long H, long long N, long long D, long long S_max, bool int8) {
     WsPlan w{};
     const long long G = H / N;
     const long long tq = kStr / G;
     const long long qtiles = (S_max + tq - 1) / tq;
-    long long parts = (qtiles + 31) / 32;
+    long long parts = (qtiles + 15) / 16;
     if (parts < 1) parts = 1;
     if (parts > kMaxParts) parts = kMaxParts;
     w.parts = static_cast<int>(parts);
