@@ -327,8 +327,10 @@ qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
  * then column mass, each recomputing the logits; summation order is the
  * kernel's).  workspace: qs_prefill_importance_workspace_size bytes, no
  * initial contents needed.  Device errors: a table entry outside
- * [0, num_kv_blocks) -> QS_DEV_EBLOCK_TABLE; S < 0 or S > min(S_max,
- * MKBPR*BS) -> QS_DEV_ESEQ_LEN, and that request's importance is left zero.
+ * [0, num_kv_blocks) -> QS_DEV_EBLOCK_TABLE (that request's importance is then
+ * unspecified; nothing outside the buffers is read or written); S < 0 or
+ * S > min(S_max, MKBPR*BS) -> QS_DEV_ESEQ_LEN, and that request's importance
+ * is left zero.
  */
 qs_status qs_prefill_importance_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D,
                                                int32_t S_max, qs_dtype kv_dtype,
