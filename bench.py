@@ -33,6 +33,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -143,7 +144,9 @@ CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.ac
 class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+        # raw samples: QS_CLOCKS_DIR if set (to keep them), else a temporary folder
+        out_dir = os.environ.get("QS_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, "clocks_rank%d.csv" % gpu_index)
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
