@@ -87,6 +87,15 @@ def test_binding_rejects_host_tensors(built_lib):
                               torch.zeros(1, 2, 4, dtype=torch.int32))
 
 
+def test_prefill_importance_binding_rejects_host_tensors(built_lib):
+    from decode_sparse_attention_gb300 import questsparse as qs
+    q = torch.zeros(1, 64, 4, 64)
+    kc = torch.zeros(4, 16, 2, 64)
+    with pytest.raises(qs.QuestSparseError, match="CUDA"):
+        qs.prefill_importance(q, kc, torch.zeros(1, 4, dtype=torch.int32),
+                              torch.zeros(1, dtype=torch.int32))
+
+
 def test_step_params_layout_matches_header():
     """The ctypes mirror of qs_step_params has the C struct's field order."""
     from decode_sparse_attention_gb300 import questsparse as qs
