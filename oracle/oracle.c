@@ -367,6 +367,96 @@ int orc_quantize_query(const void* q, int q_dt, int D, int8_t* q8, float* s_q) {
 /* a6..a8: probe / importance selector (Kestrel 10-2, §1 and §2)              */
 /* ------------------------------------------------------------------------ */
 
+/* The probe score starts from this floor before the first dot product of a
+ * block is taken into account (the engine's starting value; every block has
+ * at least one probe, so it never survives). */
+static const float PROBE_FLOOR = -1e30f;
+
+/* Positions probed in the token range [first, end) of one block: the block is
+ * sampled with a fixed stride, stride = (end - first) / n_probe tokens rounded
+ * down, at least 1, starting at the block's first token.  A full 32-token
+ * block with 8 probes is sampled at offsets 0, 4, ..., 28; a 5-token tail at
+ * every token.  Writes the positions to pos[] and returns how many. */
+static int probe_positions(int first, int end, int n_probe, int* pos) {
+    int stride = (end - first) / n_probe;
+    if (stride < 1) stride = 1;
+    int count = 0;
+    for (int p = first; p < end; p += stride) pos[count++] = p;
+    return count;
+}
+
+/* The score of one probe: q_h . K[position] for KV head kh.  Float caches: the
+ * dot product in double, rounded once to fp32.  int8 caches: the exact integer
+ * dot of the quantised query and the int8 key, scaled by s_q * s_k (two fp32
+ * roundings, as the int8 reading states). */
+static float probe_dot(const float* qf, const int8_t* q8, float s_q, const void* k_cache,
+                       const float* k_scale, int kv_dt, size_t token_row, int N, int kh, int D) {
+    const size_t base = (token_row * (size_t)N + (size_t)kh) * (size_t)D;
+    if (kv_dt == ORC_I8) {
+        long long idot = 0;
+        for (int d = 0; d < D; d++) idot += (long long)q8[d] * ((const int8_t*)k_cache)[base + d];
+        const float s_k = k_scale[token_row * (size_t)N + (size_t)kh];
+        const float s = s_q * s_k;
+        return s * (float)idot;
+    }
+    double sum = 0.0;
+    for (int d = 0; d < D; d++) sum += (double)qf[d] * dec(k_cache, kv_dt, base + d);
+    return (float)sum;
+}
+
+/* Block importance: the prefill importance of the block's tokens added up in
+ * fp32, token after token in order (the importance picks depend on these
+ * exact fp32 sums). */
+static float block_importance(const float* imp_row, int first, int end) {
+    float total = 0.0f;
+    for (int p = first; p < end; p++) total = total + imp_row[p];
+    return total;
+}
+
+/* Ranking used by both greedy passes: block a ranks before block b when its
+ * value is larger, or equal with the lower block index. */
+static int ranks_before(const float* value, int a, int b) {
+    if (value[a] != value[b]) return value[a] > value[b];
+    return a < b;
+}
+
+enum { PICK_IMPORTANCE = 1, PICK_PROBE = 2 };
+
+/* One greedy pass: up to `quota` times, take the best-ranked block not taken
+ * yet and append it to the pick list (with its origin tag).  Stops early when
+ * every block is taken: the list is never padded.  Returns the new length. */
+static int greedy_pass(const float* value, int nb, int quota, uint8_t* taken,
+                       int32_t* picks, uint8_t* origin, int n_picks, uint8_t tag) {
+    for (int round = 0; round < quota; round++) {
+        int choice = -1;
+        for (int j = 0; j < nb; j++)
+            if (!taken[j] && (choice < 0 || ranks_before(value, j, choice))) choice = j;
+        if (choice < 0) break;
+        taken[choice] = 1;
+        picks[n_picks] = choice;
+        origin[n_picks] = tag;
+        n_picks++;
+    }
+    return n_picks;
+}
+
+/* Recency insurance: the pick that makes room for the last block is the probe
+ * pick with the lowest probe score; among equal scores the larger block
+ * index (the one the greedy fill took later).  Importance picks are never
+ * candidates.  Returns its position in the pick list, or -1 if there is no
+ * probe pick. */
+static int recency_victim(const float* probe, const int32_t* picks, const uint8_t* origin,
+                          int n_picks) {
+    int victim = -1;
+    for (int i = 0; i < n_picks; i++) {
+        if (origin[i] != PICK_PROBE) continue;
+        if (victim < 0) { victim = i; continue; }
+        const float a = probe[picks[i]], b = probe[picks[victim]];
+        if (a < b || (a == b && picks[i] > picks[victim])) victim = i;
+    }
+    return victim;
+}
+
 int orc_probe_select(const void* q, int q_dt, const void* k_cache,
                      const float* k_scale, int kv_dt, int num_kv_blocks,
                      const int32_t* block_tables, int MKBPR, const int32_t* seq_lens,
@@ -376,135 +466,91 @@ int orc_probe_select(const void* q, int q_dt, const void* k_cache,
     if (k <= 0 || N <= 0 || H % N != 0 || D <= 0 || BS <= 0) return ORC_EINVAL;
     if (kv_dt == ORC_I8 && !k_scale) return ORC_EINVAL;
     if (kv_dt != ORC_I8 && !is_float_dt(kv_dt)) return ORC_EINVAL;
+    if (n_probe < 1) n_probe = 1;
     const int G = H / N;
-    const int maxnb = MKBPR;
-    float* probe = (float*)malloc(sizeof(float) * ((size_t)maxnb + 1));
-    float* imp_sum = (float*)malloc(sizeof(float) * ((size_t)maxnb + 1));
-    uint8_t* used = (uint8_t*)malloc((size_t)maxnb + 1);
-    uint8_t* is_probe_pick = (uint8_t*)malloc((size_t)k + 1);
-    int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * ((size_t)k + 1));
+    const size_t cap = (size_t)MKBPR + 1;
+    float* probe = (float*)malloc(sizeof(float) * cap);
+    float* imp = (float*)malloc(sizeof(float) * cap);
+    uint8_t* taken = (uint8_t*)malloc(cap);
+    int32_t* picks = (int32_t*)malloc(sizeof(int32_t) * ((size_t)k + 1));
+    uint8_t* origin = (uint8_t*)malloc((size_t)k + 1);
+    int* pos = (int*)malloc(sizeof(int) * ((size_t)BS + 1));
     float* qf = (float*)malloc(sizeof(float) * (size_t)D);
     int8_t* q8 = (int8_t*)malloc((size_t)D);
     int rc = ORC_OK;
-    if (!probe || !imp_sum || !used || !is_probe_pick || !sel || !qf || !q8) {
+    if (!probe || !imp || !taken || !picks || !origin || !pos || !qf || !q8) {
         rc = ORC_EINVAL;
         goto done;
     }
-    if (n_probe < 1) n_probe = 1;
     for (int b = 0; b < B; b++) {
         const int L = seq_lens[b];
         if (L < 0 || L > MKBPR * BS) { rc = ORC_EINVAL; goto done; }
         if (importance && L > S_max) { rc = ORC_EINVAL; goto done; }
-        const int n_blocks = ceil_div(L, BS);
+        const int nb = ceil_div(L, BS);
+        const int32_t* bt_row = block_tables + (size_t)b * MKBPR;
+        for (int j = 0; j < nb; j++)
+            if (bt_row[j] < 0 || bt_row[j] >= num_kv_blocks) { rc = ORC_ERANGE; goto done; }
+
+        /* signal 2: summed prefill importance per block (shared by the heads) */
+        for (int j = 0; j < nb; j++) {
+            const int first = j * BS, end = first + BS < L ? first + BS : L;
+            imp[j] = importance ? block_importance(importance + (size_t)b * S_max, first, end)
+                                : 0.0f;
+            if (imp_out) imp_out[(size_t)b * MKBPR + j] = imp[j];
+        }
+
         for (int h = 0; h < H; h++) {
             const int kh = h / G;
-            const size_t qoff = ((size_t)b * H + h) * D;
             float s_q = 0.0f;
-            for (int d = 0; d < D; d++) qf[d] = decf(q, q_dt, qoff + d);
+            for (int d = 0; d < D; d++) qf[d] = decf(q, q_dt, ((size_t)b * H + h) * D + d);
             if (kv_dt == ORC_I8) orc_quantize_query(qf, ORC_F32, D, q8, &s_q);
 
-            /* probe loop: n_probe evenly strided positions per block, block
-             * score = the largest of their dot products */
-            for (int j = 0; j < n_blocks; j++) {
-                float best = -1e30f;
-                const int p0 = j * BS;
-                int p_end = p0 + BS;
-                if (p_end > L) p_end = L;
-                int step = (p_end - p0) / n_probe;
-                if (step < 1) step = 1;
-                const int p = block_tables[(size_t)b * MKBPR + j];
-                if (p < 0 || p >= num_kv_blocks) { rc = ORC_ERANGE; goto done; }
-                for (int ps = p0; ps < p_end; ps += step) {
-                    const size_t krow = (((size_t)p * BS + (ps - p0)) * N + kh) * D;
-                    float dot;
-                    if (kv_dt == ORC_I8) {
-                        long long acc = 0;
-                        for (int d = 0; d < D; d++)
-                            acc += (long long)q8[d] * ((const int8_t*)k_cache)[krow + d];
-                        const float s_k = k_scale[((size_t)p * BS + (ps - p0)) * N + kh];
-                        dot = (s_q * s_k) * (float)acc; /* two fp32 roundings */
-                    } else {
-                        double acc = 0.0;
-                        for (int d = 0; d < D; d++)
-                            acc += (double)qf[d] * dec(k_cache, kv_dt, krow + d);
-                        dot = (float)acc;
-                    }
-                    if (dot > best) best = dot;
+            /* signal 1: the probe score of every block, the largest dot
+             * product over its probe positions */
+            for (int j = 0; j < nb; j++) {
+                const int first = j * BS, end = first + BS < L ? first + BS : L;
+                const int np = probe_positions(first, end, n_probe, pos);
+                float score = PROBE_FLOOR;
+                for (int i = 0; i < np; i++) {
+                    const size_t token_row = (size_t)bt_row[j] * BS + (size_t)(pos[i] - first);
+                    const float s = probe_dot(qf, q8, s_q, k_cache, k_scale, kv_dt, token_row, N,
+                                              kh, D);
+                    if (s > score) score = s;
                 }
-                probe[j] = best;
-                /* summed prefill importance of the block's tokens, fp32 in
-                 * token order */
-                imp_sum[j] = 0.0f;
-                if (importance)
-                    for (int ps = p0; ps < p_end; ps++)
-                        imp_sum[j] += importance[(size_t)b * S_max + ps];
-                if (probe_out) probe_out[((size_t)b * H + h) * maxnb + j] = probe[j];
-                if (imp_out && h == 0) imp_out[(size_t)b * maxnb + j] = imp_sum[j];
+                probe[j] = score;
+                if (probe_out) probe_out[((size_t)b * H + h) * MKBPR + j] = score;
             }
 
-            memset(used, 0, (size_t)n_blocks + 1);
-            int n_sel = 0;
-            /* importance pre-selection: (k+1)/2 blocks, greedy argmax of the
-             * summed importance, ties to the lower index */
-            int n_imp = 0;
-            if (importance) {
-                const int budget = (k + 1) / 2;
-                for (int i = 0; i < n_blocks && n_imp < budget; i++) {
-                    int best = -1;
-                    for (int j = 0; j < n_blocks; j++) {
-                        if (used[j]) continue;
-                        if (best < 0 || imp_sum[j] > imp_sum[best] ||
-                            (imp_sum[j] == imp_sum[best] && j < best))
-                            best = j;
-                    }
-                    if (best < 0) break;
-                    is_probe_pick[n_imp] = 0;
-                    sel[n_imp++] = best;
-                    used[best] = 1;
+            /* half of the budget, rounded up, goes to the most important
+             * blocks; the probe score fills the rest */
+            memset(taken, 0, (size_t)nb + 1);
+            int n_picks = 0;
+            if (importance)
+                n_picks = greedy_pass(imp, nb, (k + 1) / 2, taken, picks, origin, n_picks,
+                                      PICK_IMPORTANCE);
+            const int n_imp = n_picks;
+            n_picks = greedy_pass(probe, nb, k - n_picks, taken, picks, origin, n_picks,
+                                  PICK_PROBE);
+
+            /* insurance: the most recent block is always attended to, unless
+             * the budget holds no probe pick it could take the place of */
+            if (nb > 0 && !taken[nb - 1]) {
+                const int v = recency_victim(probe, picks, origin, n_picks);
+                if (v >= 0) {
+                    taken[picks[v]] = 0;
+                    picks[v] = nb - 1;
+                    taken[nb - 1] = 1;
                 }
             }
-            n_sel = n_imp;
-            /* fill the rest greedily by probe score, ties to the lower index;
-             * stop when no block is left (never pad) */
-            while (n_sel < k) {
-                int best = -1;
-                for (int j = 0; j < n_blocks; j++) {
-                    if (used[j]) continue;
-                    if (best < 0 || probe[j] > probe[best] ||
-                        (probe[j] == probe[best] && j < best))
-                        best = j;
-                }
-                if (best < 0) break;
-                is_probe_pick[n_sel] = 1;
-                sel[n_sel++] = best;
-                used[best] = 1;
-            }
-            /* recency insurance: the last block replaces the lowest-scoring
-             * probe pick (ties: the later greedy pick, i.e. the larger index);
-             * importance picks are never evicted */
-            if (n_blocks > 0 && !used[n_blocks - 1]) {
-                int worst = -1;
-                for (int i = 0; i < n_sel; i++) {
-                    if (!is_probe_pick[i]) continue;
-                    if (worst < 0 || probe[sel[i]] < probe[sel[worst]] ||
-                        (probe[sel[i]] == probe[sel[worst]] && sel[i] > sel[worst]))
-                        worst = i;
-                }
-                if (worst >= 0) {
-                    used[sel[worst]] = 0;
-                    sel[worst] = n_blocks - 1;
-                    used[n_blocks - 1] = 1;
-                }
-            }
-            qsort(sel, (size_t)n_sel, sizeof(int32_t), cmp_int32);
+
+            qsort(picks, (size_t)n_picks, sizeof(int32_t), cmp_int32);
             int32_t* out = selected + ((size_t)b * H + h) * k;
-            for (int i = 0; i < k; i++) out[i] = i < n_sel ? sel[i] : -1;
+            for (int i = 0; i < k; i++) out[i] = i < n_picks ? picks[i] : -1;
             if (n_imp_out) n_imp_out[(size_t)b * H + h] = n_imp;
         }
     }
 done:
-    free(probe); free(imp_sum); free(used); free(is_probe_pick); free(sel); free(qf);
-    free(q8);
+    free(probe); free(imp); free(taken); free(picks); free(origin); free(pos); free(qf); free(q8);
     return rc;
 }
 
