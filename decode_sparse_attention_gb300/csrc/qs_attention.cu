@@ -51,7 +51,7 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
                            int32_t k, float softmax_scale, int32_t B, int32_t H, int32_t N,
                            int32_t D, int32_t BS, float* out, float* lse_opt, void* workspace,
                            size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream,
-                           bool pdl) {
+                           bool pdl, bool clear_counters) {
     if (B < 0 || H <= 0 || N <= 0 || H % N != 0 || BS <= 0 || k <= 0 || MKBPR < 0 ||
         num_kv_blocks <= 0)
         return QS_EINVAL;
@@ -110,6 +110,11 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
     a.counters = reinterpret_cast<uint32_t*>(ws);
     a.partial = reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(units) * 4, 256));
     a.dev_status = dev_status;
+    // every check has passed: only now may the call touch the workspace
+    if (clear_counters &&
+        cudaMemsetAsync(a.counters, 0, static_cast<size_t>(units) * sizeof(uint32_t), stream) !=
+            cudaSuccess)
+        return QS_ECUDA;
     switch (kv_dtype) {
         case QS_F32: return D == 128 ? dispatch_g<Dt::F32, 128>(G, a, pl, pdl, stream)
                                      : dispatch_g<Dt::F32, 64>(G, a, pl, pdl, stream);
@@ -137,5 +142,5 @@ extern "C" qs_status qs_sparse_decode_attn(const void* q, qs_dtype q_dtype, cons
                                 num_kv_blocks, block_tables, MKBPR, seq_lens, selected, sel_heads,
                                 k, softmax_scale, B, H, N, D, BS, out, lse_opt, workspace,
                                 workspace_bytes, dev_status, reinterpret_cast<cudaStream_t>(stream),
-                                false);
+                                false, false);
 }

@@ -18,12 +18,13 @@
 // a device outside of any stream capture.
 //
 // Every call on a device uses the same array and it keeps what the previous
-// call left there, so each call first clears the arrival counters it is going
-// to use (a memset enqueued on the caller's stream).  Two calls whose work
-// overlaps on the GPU -- e.g. on two streams without ordering between them --
-// race on the array and give wrong results; order such calls on one stream.
-// The call allocates nothing: no cudaMalloc, no cudaFree, no library routine
-// that allocates.
+// call left there, so each call clears the arrival counters it is going to
+// use (a memset enqueued on the caller's stream once every argument check has
+// passed; a rejected call enqueues nothing).  Two calls whose work overlaps on
+// the GPU -- e.g. on two streams without ordering between them -- race on the
+// array and give wrong results; order such calls on one stream.  The call
+// allocates nothing: no cudaMalloc, no cudaFree, no library routine that
+// allocates.
 #include <mutex>
 
 #include "qs_internal.cuh"
@@ -32,9 +33,11 @@ namespace qs {
 
 namespace {
 
-// Maximum scratch of one call: 4 MiB.  Enough for B*sel_heads up to about
-// 990 units at H/N = 4, D = 128 (the scratch holds one arrival counter per
-// unit and up to units + 1024 partial slots of G*(D+2) floats).
+// Maximum scratch of one call: 4 MiB.  A call needs one 4-byte arrival
+// counter per unit (rounded up to 256 bytes) plus 2 * units + 1024 partial
+// slots of G * (D + 2) floats (the same formula as the workspace entry
+// point), so at H/N = 4, D = 128 (2080-byte slots) it serves at most 495
+// (request, KV head) units; 496 units already need 4,195,328 bytes.
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;
 
 __device__ __align__(256) uint8_t g_attn_scratch[kStaticScratchBytes];
@@ -73,13 +76,21 @@ extern "C" qs_status qs_sparse_decode_attn_noalloc(
     if (need > kStaticScratchBytes) return QS_EWORKSPACE;  // beyond the fixed 4 MiB scratch
     void* scratch = scratch_on_current_device();
     if (!scratch) return QS_ECUDA;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the arrival counters (the first B*sel_heads words) must start at zero;
-    // the partial slots are written before they are read
-    const size_t counters = static_cast<size_t>(B) * sel_heads * sizeof(uint32_t);
-    if (cudaMemsetAsync(scratch, 0, counters, s) != cudaSuccess) return QS_ECUDA;
+    // the arrival counters must start at zero: sparse_attn_impl clears them
+    // on the stream after its checks; the partial slots are written before
+    // they are read
     return sparse_attn_impl(q, q_dtype, k_cache, v_cache, k_scale, v_scale, kv_dtype,
                             num_kv_blocks, block_tables, MKBPR, seq_lens, selected, sel_heads, k,
                             softmax_scale, B, H, N, D, BS, out, lse_opt, scratch,
-                            kStaticScratchBytes, dev_status, s, false);
+                            kStaticScratchBytes, dev_status, reinterpret_cast<cudaStream_t>(stream),
+                            /*pdl=*/false, /*clear_counters=*/true);
+}
+
+extern "C" qs_status qs_sparse_decode_attn_noalloc_scratch(void** device_ptr, size_t* bytes) {
+    if (!device_ptr || !bytes) return QS_EINVAL;
+    void* p = qs::scratch_on_current_device();
+    if (!p) return QS_ECUDA;
+    *device_ptr = p;
+    *bytes = qs::kStaticScratchBytes;
+    return QS_OK;
 }

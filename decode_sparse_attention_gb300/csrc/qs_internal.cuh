@@ -27,7 +27,9 @@ qs_status probe_select_impl(const void* q, qs_dtype q_dtype, const void* k_cache
 
 // pdl: launch as a programmatic dependent of the kernel before it on the
 // stream (only when that kernel writes nothing the attention reads before
-// its grid-dependency wait, i.e. after the selectors).
+// its grid-dependency wait, i.e. after the selectors).  clear_counters: zero
+// the workspace's arrival counters on the stream first (after every argument
+// and plan check passed), for a workspace whose contents are unknown.
 qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
                            const void* v_cache, const float* k_scale, const float* v_scale,
                            qs_dtype kv_dtype, int32_t num_kv_blocks, const int32_t* block_tables,
@@ -35,7 +37,7 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
                            int32_t sel_heads, int32_t k, float softmax_scale, int32_t B, int32_t H,
                            int32_t N, int32_t D, int32_t BS, float* out, float* lse_opt,
                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                           cudaStream_t stream, bool pdl);
+                           cudaStream_t stream, bool pdl, bool clear_counters = false);
 
 // Fused Quest decode step (one kernel).  Sets *taken = false, and enqueues
 // nothing, when the sizes are outside what the fused kernel serves or the

@@ -88,7 +88,7 @@ typedef enum {
     QS_DEV_ESEQ_LEN = 3,      /* seq_len < 0 or > MKBPR*BS (or metadata slots)  */
     QS_DEV_ESELECTED = 4,     /* selected index >= ceil(seq_len/BS)             */
     QS_DEV_EFORCED = 5,       /* more forced window blocks than k               */
-    QS_DEV_ETIMEOUT = 6       /* a bounded device-side wait ran out             */
+    QS_DEV_ETIMEOUT = 6       /* reserved: no kernel of this version waits      */
 } qs_dev_code;
 
 typedef enum {
@@ -216,7 +216,7 @@ qs_status qs_probe_select(const void* q, qs_dtype q_dtype, const void* k_cache,
  * lse_opt: NULL or [B, H] fp32 natural-log log-sum-exp of the logits.  An
  * empty T gives out = 0 and lse = -inf.  Split-K over the selected blocks; the
  * partial results are merged on the device (no host round trip).
- * D in {64, 128}; BS a multiple of 16, <= 256; H/N (sel_heads == N) in {1,2,4}.
+ * D in {64, 128}; BS a multiple of 16, <= 4096; H/N (sel_heads == N) in {1,2,4}.
  */
 qs_status qs_sparse_decode_attn(const void* q, qs_dtype q_dtype, const void* k_cache,
                                 const void* v_cache, const float* k_scale, const float* v_scale,
@@ -235,15 +235,19 @@ qs_status qs_sparse_decode_attn(const void* q, qs_dtype q_dtype, const void* k_c
  * nothing like it; it exists for those callers.  Same arguments, layouts,
  * results and device-side error reporting as qs_sparse_decode_attn.
  *  - Scratch comes from one fixed 4 MiB array in device memory that the
- *    library holds on every GPU that loads it, until the process exits.  Sizes
- *    that need more (attention workspace above 4 MiB, i.e. more than about 990
- *    (request, KV head) units at H/N = 4, D = 128) return QS_EWORKSPACE.
+ *    library holds on every GPU that loads it, until the process exits.  A
+ *    call needs qs_workspace_size(QS_OP_SPARSE_ATTN, ...) bytes of it: 256
+ *    bytes per 64 units of arrival counters plus 2*units + 1024 partial slots
+ *    of G*(D+2) floats (units = B*sel_heads, G = H/N when sel_heads == N, else
+ *    1).  At H/N = 4, D = 128 that admits at most 495 (request, KV head)
+ *    units; sizes that need more than 4 MiB return QS_EWORKSPACE.
  *  - The first call on a device looks up the array's device address; make
  *    that first call outside of any stream capture.
- *  - Every call clears the part of the array that must start at zero (an
- *    async memset on `stream`), then runs the attention.  All calls on a
- *    device share the array: calls that overlap on the GPU race -- keep them
- *    on one stream.
+ *  - Once every argument check has passed, a call clears the part of the
+ *    array that must start at zero (an async memset on `stream`), then runs
+ *    the attention; a rejected call enqueues nothing.  All calls on a device
+ *    share the array: calls that overlap on the GPU race -- keep them on one
+ *    stream.
  *  - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
  */
 qs_status qs_sparse_decode_attn_noalloc(const void* q, qs_dtype q_dtype, const void* k_cache,
@@ -255,6 +259,14 @@ qs_status qs_sparse_decode_attn_noalloc(const void* q, qs_dtype q_dtype, const v
                                         float softmax_scale, int32_t B, int32_t H, int32_t N,
                                         int32_t D, int32_t BS, float* out, float* lse_opt,
                                         int32_t* dev_status, qs_stream_t stream);
+
+/* Where the fixed scratch of qs_sparse_decode_attn_noalloc lives on the
+ * current device: its device address and its size in bytes (looked up on the
+ * first use on a device, like the entry point's first call; allocates
+ * nothing).  For callers that want to check the size limit or inspect the
+ * array; writing to it between calls is allowed, writing while a call runs
+ * races with that call. */
+qs_status qs_sparse_decode_attn_noalloc_scratch(void** device_ptr, size_t* bytes);
 
 /* One decode step: block selection followed by the sparse attention.  Quest
  * mode reads maxblocks/minblocks/meta tables and writes selected [B, N, k];
