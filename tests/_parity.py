@@ -81,3 +81,60 @@ def quest_reference(x, w, q_dt=None):
 
 def forced_flags(L, BS, t, nb):
     return oracle.forced_set(int(L), BS, t, nb)
+
+
+def check_quest_rows(w, x, gsel, osel, osf, what=""):
+    """The gap rule on every (request, KV head) row of a Quest selection;
+    returns how many rows equal the oracle's exactly."""
+    L = to_np(x["seq_lens"])
+    exact = 0
+    for b in range(gsel.shape[0]):
+        nb = x["nb"][b]
+        fixed = forced_flags(L[b], w.BS, x["t"], nb)
+        for n in range(w.N):
+            exact += check_one_selection(gsel[b, n], osel[b, n], osf[b, n, :nb], nb, w.k, fixed,
+                                         (what, b, n))
+    return exact
+
+
+def probe_fixed(w, nb, oimp_row, n_imp):
+    """Blocks a probe selection holds regardless of the probe scores: the
+    importance picks (bit-exact fp32 sums) and, once a probe pick exists,
+    the most recent block."""
+    imp_picks = sorted(range(nb), key=lambda j: (-oimp_row[j], j))[:n_imp] if n_imp else []
+    fixed = np.zeros(nb, bool)
+    fixed[imp_picks] = True
+    if w.k > n_imp and nb > n_imp:
+        fixed[nb - 1] = True
+    return fixed
+
+
+def check_probe_rows(w, x, gsel, osel, oprobe, oimp, onimp, what=""):
+    """The gap rule on every (request, query head) row of a probe selection
+    (bit-exact for int8 caches, whose probe scores are exact integer dots)."""
+    exact = 0
+    for b in range(gsel.shape[0]):
+        nb = x["nb"][b]
+        for h in range(w.H):
+            if w.kv_dtype == "i8":
+                assert np.array_equal(gsel[b, h], osel[b, h]), (what, b, h)
+                exact += 1
+                continue
+            fixed = probe_fixed(w, nb, oimp[b], int(onimp[b, h]))
+            exact += check_one_selection(gsel[b, h], osel[b, h], oprobe[b, h, :nb], nb, w.k,
+                                         fixed, (what, b, h))
+    return exact
+
+
+def oracle_attention(x, w, sel):
+    """The oracle's attention over a given selection ([B, N or H, k])."""
+    return oracle.sparse_attention(to_np(x["q"]), DT_OF[x["q"].dtype], to_np(x["k_cache"]),
+                                   to_np(x["v_cache"]), DT_OF[x["k_cache"].dtype],
+                                   to_np(x["block_tables"]), to_np(x["seq_lens"]),
+                                   np.ascontiguousarray(sel, np.int32), w.N,
+                                   k_scale=to_np(x["k_scale"]) if "k_scale" in x else None,
+                                   v_scale=to_np(x["v_scale"]) if "v_scale" in x else None)
+
+
+DT_OF = {torch.float32: oracle.F32, torch.bfloat16: oracle.BF16, torch.float16: oracle.F16,
+         torch.int8: oracle.I8}

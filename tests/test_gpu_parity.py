@@ -12,7 +12,8 @@ import torch
 
 import oracle
 from _common import odt, to_np
-from _parity import check_one_selection, check_scores, forced_flags, quest_reference
+from _parity import (check_one_selection, check_probe_rows, check_quest_rows, check_scores,
+                     forced_flags, oracle_attention, quest_reference)
 from decode_sparse_attention_gb300 import questsparse as qs
 from decode_sparse_attention_gb300 import synth
 
@@ -242,23 +243,7 @@ def test_probe_select_parity(name):
         x, g = make(w, seed=seed)
         gsel = run_probe(w, x, g)
         osel, oprobe, oimp, onimp = probe_reference(w, x)
-        exact_required = w.kv_dtype == "i8"   # integer dots: bit-exact scores
-        for b in range(w.B):
-            nb = x["nb"][b]
-            for h in range(w.H):
-                if exact_required:
-                    assert np.array_equal(gsel[b, h], osel[b, h]), (name, seed, b, h)
-                    continue
-                # importance picks are bit-exact (same fp32 sums); the probe
-                # part follows the gap rule
-                n_imp = int(onimp[b, h])
-                imp_picks = sorted(range(nb), key=lambda j: (-oimp[b, j], j))[:n_imp] if n_imp else []
-                fixed = np.zeros(nb, bool)
-                fixed[imp_picks] = True
-                if w.k > n_imp and nb > n_imp:
-                    fixed[nb - 1] = True     # recency: the last block is always kept
-                check_one_selection(gsel[b, h], osel[b, h], oprobe[b, h, :nb], nb, w.k, fixed,
-                                    (name, seed, b, h))
+        check_probe_rows(w, x, gsel, osel, oprobe, oimp, onimp, (name, seed))
         if w.needle:
             _, j, _ = x["needle"]
             for n in range(w.N):
@@ -383,24 +368,23 @@ def test_decode_step_parity(name):
                             metadata_block_tables=g["meta_block_tables"],
                             tokens_since_metadata_update=x["t"], importance=g.get("importance"),
                             n_probe=w.n_probe, k_scale=g.get("k_scale"), v_scale=g.get("v_scale"))
+    if mode == 0:
+        _, _, osel, osf, *_ = quest_reference(x, w)
+    else:
+        osel, oprobe, oimp, onimp = probe_reference(w, x)
     for _ in range(2):   # twice: the workspace counters must rearm
         qs.sparse_decode_step(p, DEV)
         sync_ok()
         gsel = sel.cpu().numpy()
+        # every row: the selection follows the gap rule, and the attention
+        # equals the oracle's attention over the selection the GPU made
         if mode == 0:
-            _, _, osel, osf, *_ = quest_reference(x, w)
+            check_quest_rows(w, x, gsel, osel, osf, name)
         else:
-            osel, *_ = probe_reference(w, x)
-        same = np.all(gsel == osel, axis=2)
-        assert same.mean() >= 0.9, (name, same.mean())
-        oout, _ = oracle.sparse_attention(to_np(x["q"]), odt(x["q"]), to_np(x["k_cache"]),
-                                          to_np(x["v_cache"]), odt(x["k_cache"]),
-                                          to_np(x["block_tables"]), to_np(x["seq_lens"]), osel, w.N,
-                                          k_scale=to_np(x["k_scale"]) if "k_scale" in x else None,
-                                          v_scale=to_np(x["v_scale"]) if "v_scale" in x else None)
-        head_same = same if mode == 1 else np.repeat(same, w.G, axis=1)
-        err = np.abs(out.cpu().numpy() - oout)[head_same]
-        assert err.max() <= attn_tol(x["k_cache"].dtype), (name, err.max())
+            check_probe_rows(w, x, gsel, osel, oprobe, oimp, onimp, name)
+        oout, _ = oracle_attention(x, w, gsel)
+        err = np.abs(out.cpu().numpy() - oout).max()
+        assert err <= attn_tol(x["k_cache"].dtype), (name, err)
 
 
 # ---------------------------------------------------------------------------
