@@ -5,6 +5,11 @@ probe/importance selector) followed by the split-K sparse attention, enqueued
 through the C ABI (qs_sparse_decode_step) and replayed as a CUDA graph.  The
 metadata prefill is set-up, timed separately and reported on its own.
 
+The headline workload (default: the ragged batch, B=64 requests of 2K-128K
+tokens, the largest configuration) gives the contract keys (value, roofline,
+e2e, cpu_baseline, clocks, gpu_launches); every workload of --configs is then
+measured the same way and reported as its own record under "configs".
+
 Timing: the step is captured as a CUDA graph for each of R input sets
 (same shapes and lengths, other seeds), R chosen so that one rotation moves
 more than 3x the 129 MB L2; W warm-up steps, then K steps replayed back to
@@ -18,9 +23,10 @@ torchrun every rank runs an independent replica (the path needs no
 collective) and the slowest rank's time is reported.
 
 JSON line keys: metric, value (us per step, lower is better), unit, roofline
-(attention kernel vs the measured HBM copy bandwidth), cpu_baseline (the
-reference oracle on the host, bounded sample), e2e (the same step through the
-C ABI from pinned host buffers, copies included), clocks, gpu_launches.
+(attention kernel vs the measured HBM copy bandwidth), selector (its own
+bytes and rate), cpu_baseline (the reference oracle on the host, bounded
+sample, with the CPU model and core count), e2e (the same step through the C
+ABI from pinned host buffers, copies included), clocks, gpu_launches, configs.
 """
 from __future__ import annotations
 
@@ -401,18 +407,57 @@ def capture(fn, stream):
     return g
 
 
-def run_ours(args, w):
+def host_cpu():
+    """CPU model and logical core count of this host (for the CPU baseline)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": model or "unknown", "nproc": os.cpu_count()}
+
+
+def committed_selector_traffic(workload: str):
+    """dram read+write bytes of the selector kernels of one step from the
+    committed ncu summary, if taken on the current selector source."""
+    p = os.path.join(ROOT, "profiles", "sparse_attn_%s.md" % workload)
+    try:
+        txt = open(p).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"selector_source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_val = re.search(r"selector_dram_bytes_per_step:\s*([0-9]+)", txt)
+    if not m_hash or not m_val or m_hash.group(1) != selector_source_hash():
+        return None
+    return int(m_val.group(1))
+
+
+def selector_source_hash():
+    h = hashlib.sha256()
+    for f in ("qs_select.cu", "qs_probe.cu", "qs_topk.cuh", "qs_quest_score.cuh", "qs_common.cuh"):
+        with open(os.path.join(ROOT, "decode_sparse_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
+    """Times one workload's decode step (and its selector and attention
+    alone); returns its record.  headline: also the metadata update and the
+    prefill importance producer."""
     from decode_sparse_attention_gb300 import questsparse as qs
-    ws_, rank, local = dist_env()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    if ws_ > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    qs.lib()
-    stream = torch.cuda.Stream(dev)
-    flush = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    sink = torch.zeros((), dtype=torch.int64, device=dev)
 
     # input set 0, its step bytes, then as many more sets (same lengths, other
     # seeds) as it takes for the rotation to exceed 3x the L2
@@ -437,8 +482,9 @@ def run_ours(args, w):
     g_step, g_sel, g_attn = [], [], []
     keep = []   # buffers the captured graphs write into must outlive them
     for (x, _, sel, out, params, _) in sets:
-        g_step.append(capture(lambda: qs.sparse_decode_step(params, dev), stream))
+        g_step.append(capture(lambda params=params: qs.sparse_decode_step(params, dev), stream))
         sel2 = torch.empty_like(sel)
+
         def run_selector(x=x, sel2=sel2):
             if mode == 0:
                 qs.quest_block_select_paged_in_out_w(x["q"], x["maxblocks"], x["minblocks"],
@@ -450,6 +496,7 @@ def run_ours(args, w):
                                 k_scale=x.get("k_scale"), selected=sel2)
         g_sel.append(capture(run_selector, stream))
         attn_out = torch.empty_like(out)
+
         def run_attn(x=x, sel=sel, attn_out=attn_out):
             qs.sparse_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
                                   x["seq_lens"], sel, k_scale=x.get("k_scale"),
@@ -461,7 +508,7 @@ def run_ours(args, w):
     per_set = [step_bytes(w, s[0], s[2].cpu().numpy(), q_es) for s in sets]
     nbytes = {k: int(round(sum(d[k] for d in per_set) / len(per_set))) for k in per_set[0]}
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index or 0)
     t_end = time.time() + args.preroll_s
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -521,26 +568,16 @@ def run_ours(args, w):
 
     peak, peak_kind = hbm_peak()
     achieved = nbytes["attention"] / (attn_us * 1e-6) / 1e9
+    sel_gbs = nbytes["select"] / (sel_us * 1e-6) / 1e9
     kernels = qs.step_kernels(params0)
-    res = {
-        "metric": METRIC,
-        "value": round(step_us_max, 3),
-        "unit": UNIT,
-        "n_gpus": ws_,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(step_us_max / 1000.0, 6),
-        "higher_is_better": False,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16",
-                  torch.int8: "i8"}[x0["k_cache"].dtype],
-        "data": "synthetic",
+    rec = {
+        "workload": w.name,
         "config": {
             "workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "block_size": w.BS,
             "seq_len": w.seq_len if w.seq_len else "ragged", "k": w.k,
             "tokens_since_metadata_update": x0["t"], "selector": w.mode,
-            "parallelism": "replicas" if ws_ > 1 else "single GPU",
+            "n_probe": w.n_probe if w.mode == "probe" else None,
+            "kv_dtype": w.kv_dtype, "q_dtype": w.q_dtype,
             "l2": ("inputs larger than L2: %d input sets (same lengths, other seeds) replayed in "
                    "rotation, %.0f MB of step traffic per rotation vs %d MB of L2"
                    % (len(sets), len(sets) * nbytes["step"] / 1e6, l2_bytes(dev) >> 20))
@@ -551,6 +588,9 @@ def run_ours(args, w):
             "fused_select": args.fused_select,
             "kernels_per_step": kernels,
         },
+        "dtype": {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16",
+                  torch.int8: "i8"}[x0["k_cache"].dtype],
+        "us_per_step": round(step_us_max, 3),
         "step_gbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9, 1),
         "step_frac_of_peak": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / peak, 4),
         "step_frac_of_8tbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / 8000.0, 4),
@@ -569,7 +609,17 @@ def run_ours(args, w):
             "launch_us": round(attn_us, 3),
             "bytes_per_launch": nbytes["attention"],
         },
-        "selector_alone_us": round(sel_us, 3),
+        "selector": {
+            "kernels": ("quest_select_unit_kernel" if w.mode == "quest" and
+                        x0["meta_block_tables"].shape[1] * w.BS <= 128
+                        else "quest_scan_kernel + quest_unit_topk_kernel" if w.mode == "quest"
+                        else "probe_select_kernel"),
+            "us": round(sel_us, 3),
+            "bytes": nbytes["select"],
+            "achieved_gbs": round(sel_gbs, 1),
+            "frac": round(sel_gbs / peak, 4),
+            "traffic": committed_selector_traffic(w.name),
+        },
         "metadata_prefill_us": None if meta_ms is None else round(meta_ms * 1000, 2),
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -577,25 +627,82 @@ def run_ours(args, w):
         "gpu_launches": kernels * args.steps,
     }
     if meta_ms is not None:
-        upd_us, upd_bytes = metadata_update(w, x0, dev, flush, sink)
-        res["metadata_update_us"] = round(upd_us, 2)
-        res["metadata_update_gbs"] = round(upd_bytes / (upd_us * 1e-6) / 1e9, 1)
-        res["metadata_update"] = ("one decoded block per request: rows rebuilt since "
-                                  "meta_len - BS, one update after an L2 flush, %d bytes" % upd_bytes)
         L = x0["meta_seq_lens"].cpu().numpy()
         kbytes = int(sum(int(l) for l in L)) * w.N * w.D * elem_bytes(x0["k_cache"].dtype)
         mrows = sum(((int(l) + w.BS - 1) // w.BS + w.BS - 1) // w.BS * w.BS
                     for l in x0["seq_lens"].cpu().numpy())
         mbytes = mrows * w.N * w.D * elem_bytes(x0["k_cache"].dtype) * 2
-        res["metadata_prefill_gbs"] = round((kbytes + mbytes) / (meta_ms * 1e-3) / 1e9, 1)
+        rec["metadata_prefill_gbs"] = round((kbytes + mbytes) / (meta_ms * 1e-3) / 1e9, 1)
+        if headline:
+            upd_us, upd_bytes = metadata_update(w, x0, dev, flush, sink)
+            rec["metadata_update_us"] = round(upd_us, 2)
+            rec["metadata_update_gbs"] = round(upd_bytes / (upd_us * 1e-6) / 1e9, 1)
+            rec["metadata_update"] = ("one decoded block per request: rows rebuilt since "
+                                      "meta_len - BS, one update after an L2 flush, %d bytes"
+                                      % upd_bytes)
+    if rank == 0 and cpu_seconds > 0:
+        rec["cpu_baseline"] = cpu_baseline(w, x0, cpu_seconds)
+    del sets, keep, g_step, g_sel, g_attn
+    return rec
+
+
+SUB_CONFIGS = "bf16_paged,fp16_paged,probe_importance,probe_importance_i8,long_context"
+
+
+def run_ours(args, w):
+    from decode_sparse_attention_gb300 import questsparse as qs
+    ws_, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    qs.lib()
+    stream = torch.cuda.Stream(dev)
+    flush = torch.zeros(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    cpu = 0 if args.no_cpu_baseline else args.cpu_seconds
+    head = measure(args, w, dev, stream, flush, sink, rank, cpu, headline=True)
+    torch.cuda.empty_cache()
+    subs = {}
+    names = [n for n in (args.configs.split(",") if args.configs else []) if n and n != w.name]
+    for name in names:
+        sub_cpu = 0 if args.no_cpu_baseline else args.sub_cpu_seconds
+        subs[name] = measure(args, synth.WORKLOADS[name], dev, stream, flush, sink, rank, sub_cpu,
+                             headline=False)
+        torch.cuda.empty_cache()
+
+    res = {
+        "metric": METRIC,
+        "value": head["us_per_step"],
+        "unit": UNIT,
+        "n_gpus": ws_,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(head["us_per_step"] / 1000.0, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": head["dtype"],
+        "data": "synthetic",
+        "config": dict(head["config"], parallelism="replicas" if ws_ > 1 else "single GPU"),
+    }
+    for k_ in ("step_gbs", "step_frac_of_peak", "step_frac_of_8tbs", "algorithmic_bytes",
+               "step_us_p10_p50_p90", "step_us_flushed_single", "roofline", "selector",
+               "metadata_prefill_us", "metadata_prefill_gbs", "metadata_update_us",
+               "metadata_update_gbs", "metadata_update", "e2e", "clocks", "gpu_launches",
+               "cpu_baseline"):
+        if k_ in head:
+            res[k_] = head[k_]
     if rank == 0 and not args.no_importance:
-        res["prefill_importance"] = prefill_importance_timing(dev, clocks)
-    if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, x0, args.cpu_seconds)
+        res["prefill_importance"] = prefill_importance_timing(dev, head["clocks"])
+    res["configs"] = subs
     if ws_ > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return res if rank == 0 else None
+
 
 
 # ---------------------------------------------------------------------------
@@ -683,9 +790,9 @@ def cpu_baseline(w, x, budget_s):
         oracle_step(w, x["t"], sub)
         times.append(time.perf_counter() - t0)
     per_step_us = statistics.median(times) * 1e6 * w.B / len(reqs)
-    return {"value": round(per_step_us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d of %d requests per step, %d runs, scaled by %d/%d to a full step"
-                      % (len(reqs), w.B, len(times), w.B, len(reqs))}
+    return dict({"value": round(per_step_us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                 "sample": "%d of %d requests per step, %d runs, scaled by %d/%d to a full step"
+                           % (len(reqs), w.B, len(times), w.B, len(reqs))}, **host_cpu())
 
 
 def run_reference(args, w):
@@ -711,8 +818,8 @@ def run_reference(args, w):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D,
                        "block_size": w.BS, "k": w.k, "selector": w.mode},
-            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": dict({"value": round(us, 1), "unit": UNIT, "cores": 1,
+                                  "kind": "oracle", "sample": sample}, **host_cpu()),
             "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -723,13 +830,19 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="bf16_paged", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="ragged", choices=sorted(synth.WORKLOADS),
+                    help="the headline workload (value, roofline, e2e)")
+    ap.add_argument("--configs", default=SUB_CONFIGS,
+                    help="comma-separated workloads measured after the headline, each reported "
+                         "as its own record under 'configs' ('' for none)")
+    ap.add_argument("--sub-cpu-seconds", type=float, default=4.0,
+                    help="oracle seconds per record under 'configs'")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-importance", action="store_true",
                     help="skip timing the prefill importance producer")
-    ap.add_argument("--max-sets", type=int, default=24,
+    ap.add_argument("--max-sets", type=int, default=32,
                     help="most input sets to rotate through; workloads needing more (tiny "
                          "steps) are timed with an L2 flush between steps instead")
     ap.add_argument("--fused-select", type=int, default=-1, choices=[-1, 0, 1],

@@ -26,6 +26,7 @@ pages report):
   ragged           bf16, B=64, seq_len ~U[2048,131072] rounded to 128 and
                    clamped to >= k*BLOCK_SIZE, shuffled shared page pool,
                    MMBPR=8, k=32, sink+window on (t=0).
+  fp16_paged       the bf16_paged shape with fp16 K, V and queries.
 Prefill queries for the importance producer (``prefill_queries``): one row
 per (position, query head) drawn like the decode query, over the same pages.
 """
@@ -93,6 +94,10 @@ WORKLOADS = {
     "ragged": Workload("ragged", B=64, H=32, N=8, D=128, BS=128, k=32,
                        ragged=(2048, 131072, 128), t=0, outlier_channels=4, k_dist="normal",
                        MMBPR=8),
+    # the bf16_paged shape in fp16 (the Ascend kernels' primary dtype)
+    "fp16_paged": Workload("fp16_paged", B=20, H=32, N=8, D=128, BS=128, k=8, seq_len=16384,
+                           t=-1, outlier_channels=4, k_dist="normal", MMBPR=1, kv_dtype=F16,
+                           q_dtype=F16),
 }
 
 
