@@ -84,7 +84,7 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
     const long long units = static_cast<long long>(B) * sel_heads;
     AttnArgs a = {};
     AttnPlan pl = {};
-    if (!plan_attention(BS, D, G, es, q_es, int8, units, k, &a, &pl)) return QS_EUNSUPPORTED;
+    if (!plan_attention(BS, D, G, es, q_es, int8, units, k, MKBPR, &a, &pl)) return QS_EUNSUPPORTED;
     if (pl.grid > units + 1024) return QS_EUNSUPPORTED;   // partial slots: grid + units
     const size_t need = attn_workspace_bytes(B, H, N, D, sel_heads);
     if (!workspace || workspace_bytes < need) return QS_EWORKSPACE;

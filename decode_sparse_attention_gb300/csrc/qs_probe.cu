@@ -18,9 +18,11 @@
 // unit of 2..8 chunks runs as a thread-block cluster whose CTAs write their
 // probe scores and importance sums into the leader CTA's shared memory
 // (larger units use global buffers and an arrival counter).  The leader then
-// selects for each query head: histogram top-k passes for the importance
-// picks and the probe fill, a min-reduction for the recency eviction, and the
-// indices written in ascending order.
+// selects for each query head: a top-k pass for the importance picks and one
+// for the probe fill (up to 256 blocks: every thread ranks one block by
+// counting, one pass over the keys; more blocks: histogram levels), a
+// min-reduction for the recency eviction, and the indices written in
+// ascending order.
 #include <cooperative_groups.h>
 
 #include "qs_internal.cuh"
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     __shared__ float s_sq[G];
     __shared__ TopkFastScratch s_fast;
     __shared__ TopkScratch<kThreads> s_topk;
-    __shared__ unsigned long long s_best;   // recency: lowest (probe key, index) pick
+    __shared__ unsigned long long s_wmin[kThreads / 32];   // recency: lowest (probe key, index) pick per warp
     __shared__ int s_last;
 
     pdl_launch_dependents();
@@ -144,7 +146,6 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         dst_pkeys = cooperative_groups::this_cluster().map_shared_rank(pkeys, 0);
         dst_ikeys = cooperative_groups::this_cluster().map_shared_rank(ikeys, 0);
     }
-    topk_fast_clear<kThreads>(s_fast, nb);
 
     // queries of the group (fp32), plus the int8 quantisation for int8 caches
     for (int i = threadIdx.x; i < G * D; i += kThreads) {
@@ -336,9 +337,18 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
 
     // ---- importance pre-selection (same for every head of the request)
     const int n_imp = a.importance ? min((a.k + 1) / 2, nb) : 0;
+    const bool small = nb <= kThreads;   // rank by counting, one pass
     for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = kCand;
     __syncthreads();
-    if (n_imp > 0) topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
+    if (n_imp > 0) {
+        if (small) {
+            topk_rank_small(ikeys, imp_flags, nb, n_imp);
+        } else if (!topk_filter(ikeys, imp_flags, nb, n_imp, s_fast)) {
+            topk_fast_clear<kThreads>(s_fast, nb);
+            __syncthreads();
+            topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
+        }
+    }
     for (int j = threadIdx.x; j < nb; j += kThreads)
         imp_flags[j] = (imp_flags[j] & kPick) ? kFixed : 0;
     const int want = min(a.k - n_imp, nb - n_imp);
@@ -347,15 +357,18 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     for (int h = 0; h < G; ++h) {
         const size_t row = static_cast<size_t>(b) * a.H + n * G + h;
         const uint32_t* keys = pkeys + static_cast<size_t>(h) * a.MKBPR;
-        topk_fast_clear<kThreads>(s_fast, nb);
         for (int j = threadIdx.x; j < nb; j += kThreads) flags[j] = imp_flags[j] ? kFixed : kCand;
         __syncthreads();
-        topk_fast<kThreads>(keys, flags, nb, want, s_fast, s_topk);
+        if (small) {
+            topk_rank_small(keys, flags, nb, want);
+        } else if (!topk_filter(keys, flags, nb, want, s_fast)) {
+            topk_fast_clear<kThreads>(s_fast, nb);
+            __syncthreads();
+            topk_fast<kThreads>(keys, flags, nb, want, s_fast, s_topk);
+        }
         if (want > 0 && !(flags[nb - 1] & (kFixed | kPick))) {
             // the last block replaces the probe pick with the lowest probe
             // score (ties: the larger index); importance picks stay
-            if (threadIdx.x == 0) s_best = ~0ull;
-            __syncthreads();
             unsigned long long mine = ~0ull;
             for (int j = threadIdx.x; j < nb; j += kThreads)
                 if (flags[j] & kPick) {
@@ -363,10 +376,18 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
                         (static_cast<unsigned long long>(keys[j]) << 32) | (0xffffffffu - static_cast<uint32_t>(j));
                     mine = c < mine ? c : mine;
                 }
-            atomicMin(&s_best, mine);
+            // minimum over the block: warp shuffles, then one thread over the warps
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xffffffffu, mine, o);
+                mine = other < mine ? other : mine;
+            }
+            if (lane == 0) s_wmin[warp] = mine;
             __syncthreads();
             if (threadIdx.x == 0) {
-                const int victim = static_cast<int>(0xffffffffu - static_cast<uint32_t>(s_best & 0xffffffffu));
+                unsigned long long best = ~0ull;
+                for (int w = 0; w < kThreads / 32; ++w) best = s_wmin[w] < best ? s_wmin[w] : best;
+                const int victim = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best & 0xffffffffu));
                 flags[victim] &= static_cast<uint8_t>(~kPick);
                 flags[nb - 1] |= kPick;
             }

@@ -28,21 +28,19 @@ namespace qs {
 
 namespace {
 
-// Selection scratch inside the ring region; false if it does not fit.
-bool plan_fused_select(int G, int D, int q_es, int k, int MMBPR, int MKBPR, int BS, long long tpu,
-                       AttnArgs* a) {
+// Selection scratch inside the ring region, after the prologue staging
+// (which must hold the block-table rows); false if it does not fit.
+bool plan_fused_select(int D, int k, int MMBPR, int BS, long long tpu, AttnArgs* a) {
     const long long upc = plan_units_per_cta(a->tpc, tpu);
     const long long rows = upc * MMBPR * BS;
-    size_t off = 0;
+    if (!a->bt_staged) return false;
+    size_t off = a->sel_end;
     auto take = [&](size_t bytes) {
         const size_t at = off;
         off = align_up(off + bytes, 16);
         return static_cast<uint32_t>(at);
     };
-    a->sel_off_qraw = take(static_cast<size_t>(upc) * G * D * q_es);
     a->sel_off_mbt = take(static_cast<size_t>(upc) * MMBPR * 4);
-    a->sel_off_bt = take(static_cast<size_t>(upc) * MKBPR * 4);
-    a->sel_off_len = take(static_cast<size_t>(upc) * 4);
     a->sel_off_qg = take(static_cast<size_t>(upc) * D * 4);
     a->sel_off_keys = take(static_cast<size_t>(rows) * 4);
     a->sel_off_flags = take(static_cast<size_t>(rows));
@@ -93,10 +91,10 @@ qs_status quest_step_fused(const qs_step_params* p, void* attn_ws, size_t attn_w
     AttnArgs a = {};
     AttnPlan pl = {};
     const int q_es = p->q_dtype == QS_F32 ? 4 : 2;
-    if (!plan_attention(BS, D, G, es, q_es, false, units, k, &a, &pl)) return QS_OK;
+    if (!plan_attention(BS, D, G, es, q_es, false, units, k, p->MKBPR, &a, &pl)) return QS_OK;
     if (pl.grid > units + 1024) return QS_OK;
     const long long tpu = static_cast<long long>(k) * a.split;
-    if (!plan_fused_select(G, D, q_es, k, p->MMBPR, p->MKBPR, BS, tpu, &a)) return QS_OK;
+    if (!plan_fused_select(D, k, p->MMBPR, BS, tpu, &a)) return QS_OK;
     const long long n_units_max = plan_units_per_cta(a.tpc, tpu);
     if (p->fused_select < 0) {
         // the fused kernel pays for the per-CTA selection before its first

@@ -163,3 +163,17 @@ def test_fused_step_reports_bad_seq_len(fused):
     torch.cuda.synchronize()
     assert qs.read_status(DEV) == 3
     assert torch.all(sel[0] == -1)
+
+
+@pytest.mark.parametrize("fused", [1, 0])
+def test_step_all_scores_tie(fused):
+    """Identical metadata rows everywhere: every block scores the same, so
+    both forms of the step take the lowest k indices (ties to the lower
+    index) and agree bit for bit."""
+    w = W["bf16_paged"].replace(B=2, seq_len=128 * 40, MMBPR=None, k=8)
+    x, g = prepare(w, 0)
+    g["maxblocks"].fill_(0.5)
+    g["minblocks"].fill_(-0.25)
+    sel, out, _ = run_step(w, x, g, fused=fused)
+    sync_ok()
+    assert np.all(sel.cpu().numpy() == np.arange(8, dtype=np.int32))
