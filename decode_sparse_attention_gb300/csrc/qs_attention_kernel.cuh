@@ -27,15 +27,15 @@
 //    warp per head reduces the warps' maxima and sums, every thread then
 //    combines its output channels).  Q.K uses 8 lanes per token and packed
 //    fp32x2 FMAs with a transposing shuffle reduction; P.V gives each lane
-//    D/32 output channels and skips the rows a partial tile does not hold, so
-//    ring bytes that were never loaded are never used in arithmetic; the
-//    accumulators are rescaled only when a head's running max grew.
+//    D/32 output channels and runs over all of a warp's rows (p = 0 past the
+//    valid ones; the ring is zeroed once per launch so those bytes are
+//    finite); the accumulators are rescaled only when a head's max grew.
 //  * A unit split across CTAs is merged on the device: each CTA writes a
 //    (max, sum, acc) partial; the last to arrive (atomic counter, no spin)
 //    combines them and rearms the counter.
 //  * Inside the decode step it is launched as a programmatic dependent of the
 //    selector: the staging copies (none of which read what the selector
-//    writes) are in flight before the grid-dependency wait.
+//    writes) and the ring zeroing happen before the grid-dependency wait.
 #pragma once
 
 #include <cmath>
@@ -361,22 +361,7 @@ QS_DEVINL void quest_select_units(const AttnArgs& a, int u_first, int n_units, i
     }
     __syncthreads();
 
-    // forced set and top-k (step 2.3 + window): units of up to blockDim.x
-    // blocks one after the other with the whole CTA ranking by counting;
-    // longer units one warp each
-    for (int us = 0; us < n_units; ++us) {
-        const int nb = s_nb[us];
-        if (nb < 0 || nb > nthreads) continue;   // uniform
-        const int w0 = forced_window_start(len_s[(u_first + us) / a.N - b_first], BS, nb, a.t);
-        const int n_forced = forced_count(nb, w0, a.t);
-        if (n_forced > a.k) continue;
-        const uint32_t* ku = keys + s_roff[us];
-        uint8_t* fu = flags + s_roff[us];
-        for (int j = tid; j < nb; j += nthreads)
-            fu[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
-        __syncthreads();
-        topk_rank_small(ku, fu, nb, min(a.k - n_forced, nb - n_forced));
-    }
+    // forced set and top-k (step 2.3 + window), one warp per unit
     for (int us = warp; us < n_units; us += nw) {
         const int u = u_first + us;
         int32_t* sel_us = sel_s + us * a.k;
@@ -389,12 +374,11 @@ QS_DEVINL void quest_select_units(const AttnArgs& a, int u_first, int n_units, i
         } else {
             const uint32_t* ku = keys + s_roff[us];
             uint8_t* fu = flags + s_roff[us];
-            if (nb > nthreads) {
-                for (int j = lane; j < nb; j += 32)
-                    fu[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
-                __syncwarp();
-                warp_topk_smem(ku, fu, nb, min(a.k - n_forced, nb - n_forced), wtk[us]);
-            }
+            for (int j = lane; j < nb; j += 32)
+                fu[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
+            __syncwarp();
+            const int want = min(a.k - n_forced, nb - n_forced);
+            warp_topk_smem(ku, fu, nb, want, wtk[us]);
             warp_emit_flags(fu, kFixed | kPick, nb, a.k, sel_us);
         }
         __syncwarp();
@@ -457,9 +441,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
     // ---- prologue: stage what the preceding kernel does not write (query
     // rows, block-table rows, lengths; fused: metadata-table rows), then wait
     // for it (the selection), then convert the queries and build the tile list
+    // ring bytes are zeroed once, so that the rows a warp never loads hold
+    // finite values: P.V runs over all of a warp's rows with p = 0 past the
+    // valid ones (the staging area at the ring's start is zeroed after use)
+    const size_t ring_bytes = static_cast<size_t>(a.NW) * S * a.stage_bytes;
+    auto zero_ring = [&](size_t lo, size_t hi) {
+        for (size_t o = lo + static_cast<size_t>(tid) * 16; o < hi; o += static_cast<size_t>(nthreads) * 16)
+            *reinterpret_cast<uint4*>(stages + o) = make_uint4(0, 0, 0, 0);
+    };
     stage_unit_inputs<D, G>(a, u_first, n_units, b_first, n_req, stages);
     if constexpr (kSel) stage_meta_tables(a, u_first, n_units, stages);
     cp_async_commit();
+    zero_ring(a.sel_end, ring_bytes);
     if constexpr (!kSel) pdl_wait();   // the selection is written by the preceding kernel
     cp_async_wait(0);
     __syncthreads();
@@ -518,6 +511,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
         info[i] = ti;
     }
     __syncthreads();   // the staging area is free from here on: the ring takes it
+    zero_ring(0, a.sel_end);
+    __syncthreads();
 
     // ---- per-warp row streams: lane -> (row within a copy step, 16-byte
     // chunk) of the warp's kRPW rows, offsets fixed for the whole loop
@@ -651,8 +646,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
             const uint8_t* vtile = cur + a.rows_bytes;
             const float* kst = reinterpret_cast<const float*>(cur + 2 * a.rows_bytes);
             const float* vst = kst + kRPW;
-            // ---- Q.K for the warp's rows (rows past rw hold stale bytes; their
-            // logits are replaced by -inf, never used arithmetically)
+            // ---- Q.K for the warp's rows (the logits of rows past rw are
+            // replaced by -inf)
             float x[qpw];
 #pragma unroll
             for (int qi = 0; qi < qpw; ++qi) {
@@ -725,10 +720,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
                 }
             }
             __syncwarp();
-            // ---- P.V over the warp's valid rows (rw is warp-uniform)
+            // ---- P.V over every row of the warp's slice: rows past rw have
+            // p = 0 and finite (zeroed or earlier) data in the ring
 #pragma unroll
             for (int r = 0; r < kRPW; ++r) {
-                if (r < rw) {
+                {
                     float v[EPL];
                     if constexpr (KT == Dt::F32) {
                         const float* vr = reinterpret_cast<const float*>(vtile + r * ROWB) + lane * EPL;

@@ -18,11 +18,9 @@
 // unit of 2..8 chunks runs as a thread-block cluster whose CTAs write their
 // probe scores and importance sums into the leader CTA's shared memory
 // (larger units use global buffers and an arrival counter).  The leader then
-// selects for each query head: a top-k pass for the importance picks and one
-// for the probe fill (up to 256 blocks: every thread ranks one block by
-// counting, one pass over the keys; more blocks: histogram levels), a
-// min-reduction for the recency eviction, and the indices written in
-// ascending order.
+// selects for each query head: histogram top-k passes for the importance
+// picks and the probe fill, a min-reduction for the recency eviction, and the
+// indices written in ascending order.
 #include <cooperative_groups.h>
 
 #include "qs_internal.cuh"
@@ -146,6 +144,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         dst_pkeys = cooperative_groups::this_cluster().map_shared_rank(pkeys, 0);
         dst_ikeys = cooperative_groups::this_cluster().map_shared_rank(ikeys, 0);
     }
+    topk_fast_clear<kThreads>(s_fast, nb);
 
     // queries of the group (fp32), plus the int8 quantisation for int8 caches
     for (int i = threadIdx.x; i < G * D; i += kThreads) {
@@ -337,18 +336,9 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
 
     // ---- importance pre-selection (same for every head of the request)
     const int n_imp = a.importance ? min((a.k + 1) / 2, nb) : 0;
-    const bool small = nb <= kThreads;   // rank by counting, one pass
     for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = kCand;
     __syncthreads();
-    if (n_imp > 0) {
-        if (small) {
-            topk_rank_small(ikeys, imp_flags, nb, n_imp);
-        } else if (!topk_filter(ikeys, imp_flags, nb, n_imp, s_fast)) {
-            topk_fast_clear<kThreads>(s_fast, nb);
-            __syncthreads();
-            topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
-        }
-    }
+    if (n_imp > 0) topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
     for (int j = threadIdx.x; j < nb; j += kThreads)
         imp_flags[j] = (imp_flags[j] & kPick) ? kFixed : 0;
     const int want = min(a.k - n_imp, nb - n_imp);
@@ -357,15 +347,10 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     for (int h = 0; h < G; ++h) {
         const size_t row = static_cast<size_t>(b) * a.H + n * G + h;
         const uint32_t* keys = pkeys + static_cast<size_t>(h) * a.MKBPR;
+        topk_fast_clear<kThreads>(s_fast, nb);
         for (int j = threadIdx.x; j < nb; j += kThreads) flags[j] = imp_flags[j] ? kFixed : kCand;
         __syncthreads();
-        if (small) {
-            topk_rank_small(keys, flags, nb, want);
-        } else if (!topk_filter(keys, flags, nb, want, s_fast)) {
-            topk_fast_clear<kThreads>(s_fast, nb);
-            __syncthreads();
-            topk_fast<kThreads>(keys, flags, nb, want, s_fast, s_topk);
-        }
+        topk_fast<kThreads>(keys, flags, nb, want, s_fast, s_topk);
         if (want > 0 && !(flags[nb - 1] & (kFixed | kPick))) {
             // the last block replaces the probe pick with the lowest probe
             // score (ties: the larger index); importance picks stay

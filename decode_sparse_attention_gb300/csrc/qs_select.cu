@@ -63,8 +63,8 @@ struct SelectArgs {
 // keys_s (shared, indexed by row) when given; scores to scores_u (global,
 // indexed by row) when given.
 template <Dt MT, int D>
-QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j_cap,
-                           const int32_t* L_ptr, uint32_t* keys_s, float* scores_u) {
+QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j_end,
+                           uint32_t* keys_s, float* scores_u) {
     constexpr int kElemBytes = DtInfo<MT>::bytes;
     constexpr int kLanesPerRow = D * kElemBytes / 16;   // 8, 16 or 32
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
@@ -80,15 +80,11 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
     // Table entries and the G heads' query slices are all requested before
     // either is used (in-order issue would otherwise serialise the round
     // trips); the metadata rows follow once the table entries are back.
-    // The request's length arrives with them: the table entries of every
-    // row the table can hold (j < j_cap) are requested, whether or not the
-    // request reaches them.
-    const int L = *L_ptr;
     int mrow[kUnroll];
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
         const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
-        mrow[r] = j < j_cap ? a.mbt[static_cast<size_t>(b) * a.MMBPR + QS_META_BLOCK(a, j)] : -1;
+        mrow[r] = j < j_end ? a.mbt[static_cast<size_t>(b) * a.MMBPR + QS_META_BLOCK(a, j)] : -1;
     }
     constexpr int kQBytes = kEl * 4;                 // fp32 query slice; 16-bit uses half
     constexpr int kQVec = (kQBytes + 15) / 16;       // 16-byte loads per head slice
@@ -138,8 +134,6 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
     }
     RowChunk<MT> rc;
     rc.prepare(qreg);
-    const int nb_l = L < 0 ? -1 : (L + BS - 1) / BS;
-    const int j_end = (nb_l < 0 || nb_l > j_cap) ? 0 : nb_l;   // a bad length loads nothing
     uint4 vmx[kUnroll], vmn[kUnroll];
     bool live[kUnroll];
 #pragma unroll
@@ -184,19 +178,12 @@ QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, const uint32_t* k
         __syncthreads();
         return;
     }
+    topk_fast_clear<kThreads>(s_fast, nb);
     for (int j = threadIdx.x; j < nb; j += kThreads)
         flags[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
     __syncthreads();
     const int want = min(a.k - n_forced, nb - n_forced);
-    // up to kThreads blocks: rank by counting; more: filter by group bests,
-    // histogram levels when the filter cannot settle the set
-    if (nb <= kThreads) {
-        topk_rank_small(keys_s, flags, nb, want);
-    } else if (!topk_filter(keys_s, flags, nb, want, s_fast)) {
-        topk_fast_clear<kThreads>(s_fast, nb);
-        __syncthreads();
-        topk_fast<kThreads>(keys_s, flags, nb, want, s_fast, s_topk);
-    }
+    topk_fast<kThreads>(keys_s, flags, nb, want, s_fast, s_topk);
     block_emit_flags<kThreads>(flags, kFixed | kPick, nb, a.k, sel_out, s_topk);
     __syncthreads();
 }
@@ -211,20 +198,18 @@ __global__ void __launch_bounds__(kThreads, 2) quest_select_unit_kernel(SelectAr
     const int u = blockIdx.x;
     const int b = u / a.N, n = u % a.N;
     const int maxnb = a.MMBPR * a.BS;
-    int32_t* sel_out = a.selected + static_cast<size_t>(u) * a.k;
-    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
-    uint8_t* flags = dyn + static_cast<size_t>(maxnb) * 4;
-    // the length, the table entries and the queries are requested together;
-    // rows past the length are not loaded
-    score_chunk<MT, D>(a, b, n, 0, maxnb, a.seq_lens + b, keys,
-                       a.scores_out ? a.scores + static_cast<size_t>(u) * maxnb : nullptr);
     const int L = a.seq_lens[b];
+    int32_t* sel_out = a.selected + static_cast<size_t>(u) * a.k;
     if (L < 0 || (L + a.BS - 1) / a.BS > maxnb) {
         if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_ESEQ_LEN);
         for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;
         return;
     }
     const int nb = (L + a.BS - 1) / a.BS;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
+    uint8_t* flags = dyn + static_cast<size_t>(maxnb) * 4;
+    score_chunk<MT, D>(a, b, n, 0, nb, keys,
+                       a.scores_out ? a.scores + static_cast<size_t>(u) * maxnb : nullptr);
     __syncthreads();
     select_unit(a, L, nb, keys, flags, sel_out, s_fast, s_topk);
 }
@@ -450,16 +435,13 @@ __global__ void __launch_bounds__(kThreads) quest_unit_topk_kernel(SelectArgs a)
     extern __shared__ __align__(16) uint8_t dyn[];   // keys [maxnb] u32, flags [maxnb] u8
     __shared__ TopkFastScratch s_fast;
     __shared__ TopkScratch<kThreads> s_topk;
+    pdl_launch_dependents();
     const int u = blockIdx.x;
     const int b = u / a.N;
     const int maxnb = a.MMBPR * a.BS;
     const int L = a.seq_lens[b];
     int32_t* sel_out = a.selected + static_cast<size_t>(u) * a.k;
     pdl_wait();   // the scores are written by the scan
-    // Only now let the attention launch: triggered at the start, its CTAs
-    // (which need a whole SM each) would take the SMs the scan frees before
-    // this kernel's remaining CTAs get them.
-    pdl_launch_dependents();
     if (L < 0 || (L + a.BS - 1) / a.BS > maxnb) {
         if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_ESEQ_LEN);
         for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;

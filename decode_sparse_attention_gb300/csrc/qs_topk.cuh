@@ -86,8 +86,6 @@ struct TopkFastScratch {
     uint32_t wmax[32], wmin[32];
     int wcnt[32];
     int nlist, dstar, remaining, inbin;
-    unsigned long long thr;   // topk_filter: bound on the want-th best entry
-    int ncand;                // topk_filter: entries at least as good as thr
 };
 
 // Clears the histogram copies a top-k over n keys uses; call before
@@ -342,123 +340,6 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
             ++before;
         }
     __syncthreads();
-}
-
-// Top-k by counting, for n <= blockDim.x entries.  Entry j is ranked among
-// the kCand entries (key descending, lower index first) by a group of p
-// consecutive threads (p = the largest power of two <= 32 with 2*p*n <=
-// blockDim.x, else 1), each comparing it with every p-th run of four keys
-// into four independent counters; the group's counts are added with
-// shuffles and kPick is set when the rank is below want.  Exact; all threads
-// call it; ends with a barrier.  Cheaper than the histogram levels while n
-// is a few hundred at most.
-QS_DEVINL void topk_rank_small(const uint32_t* keys, uint8_t* flags, int n, int want) {
-    const int nt = static_cast<int>(blockDim.x), tid = threadIdx.x;
-    int p = 1;
-    while (p < 32 && 2 * p * n <= nt) p *= 2;
-    const int j = tid / p, part = tid & (p - 1);
-    const bool mine = want > 0 && j < n && (flags[j] & kCand);
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-    if (mine) {
-        const uint32_t kj = keys[j];
-        const bool vec = ((reinterpret_cast<uintptr_t>(keys) & 15) |
-                          (reinterpret_cast<uintptr_t>(flags) & 3)) == 0;
-        const int n4 = vec ? (n & ~3) : 0;
-        for (int i = 4 * part; i < n4; i += 4 * p) {
-            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
-            const uint32_t f4 = *reinterpret_cast<const uint32_t*>(flags + i);
-            r0 += ((f4 & kCand) != 0) && (k4.x > kj || (k4.x == kj && i < j));
-            r1 += ((f4 & (kCand << 8)) != 0) && (k4.y > kj || (k4.y == kj && i + 1 < j));
-            r2 += ((f4 & (kCand << 16)) != 0) && (k4.z > kj || (k4.z == kj && i + 2 < j));
-            r3 += ((f4 & (kCand << 24)) != 0) && (k4.w > kj || (k4.w == kj && i + 3 < j));
-        }
-        for (int i = n4 + part; i < n; i += p)
-            r0 += (flags[i] & kCand) && (keys[i] > kj || (keys[i] == kj && i < j));
-    }
-    int rank = (r0 + r1) + (r2 + r3);
-    for (int o = 1; o < p; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    const bool pick = mine && part == 0 && rank < want;
-    __syncthreads();
-    if (pick) flags[j] |= kPick;
-    __syncthreads();
-}
-
-// Top-k by filtering, for want small next to n.  Entries are ordered by
-// one 64-bit composite (key, then the complement of the index: key
-// descending, lower index first; entries not flagged kCand compose to 0).
-// The best entry of every group of g consecutive entries (g = 8, smaller
-// when that would leave fewer than want groups) bounds the want-th best
-// entry from below: at least want entries are as good as T, the want-th best
-// of the group bests.  Only the entries as good as T -- want of them at
-// least, usually not many more -- are ranked, by counting.  Returns false,
-// with the flags untouched, when it cannot settle the set within its
-// scratch (more than 512 groups or candidates, or fewer than want groups
-// holding a candidate); the caller then runs the histogram levels, after
-// topk_fast_clear (the scratch is shared).  All threads; ends with a barrier.
-QS_DEVINL bool topk_filter(const uint32_t* keys, uint8_t* flags, int n, int want,
-                           TopkFastScratch& s) {
-    constexpr int kCap = 512;
-    const int tid = threadIdx.x, nt = static_cast<int>(blockDim.x), lane = tid & 31;
-    unsigned long long* gbest = reinterpret_cast<unsigned long long*>(&s.hist[0][0]);
-    unsigned long long* cand = gbest + kCap;
-    static_assert(sizeof(s.hist) >= 2 * kCap * sizeof(unsigned long long), "filter scratch");
-    if (want <= 0) return true;
-    int g = 8;
-    while (g > 1 && (n + g - 1) / g < want) g >>= 1;
-    const int m = (n + g - 1) / g;
-    if (m > kCap) return false;
-    auto ck = [&](int j) -> unsigned long long {
-        return (flags[j] & kCand) ? ((static_cast<unsigned long long>(keys[j]) << 32) |
-                                     (0xffffffffu - static_cast<uint32_t>(j)))
-                                  : 0ull;
-    };
-    if (tid == 0) {
-        s.thr = 0ull;
-        s.ncand = 0;
-    }
-    for (int t = tid; t < m; t += nt) {
-        unsigned long long best = 0ull;
-        const int j1 = min(n, t * g + g);
-        for (int j = t * g; j < j1; ++j) {
-            const unsigned long long v = ck(j);
-            best = v > best ? v : best;
-        }
-        gbest[t] = best;
-    }
-    __syncthreads();
-    for (int t = tid; t < m; t += nt) {
-        const unsigned long long v = gbest[t];
-        if (v == 0ull) continue;
-        int rank = 0;
-        for (int u = 0; u < m; ++u) rank += gbest[u] > v;
-        if (rank == want - 1) s.thr = v;   // the composites are distinct
-    }
-    __syncthreads();
-    const unsigned long long T = s.thr;
-    if (T == 0ull) return false;
-    const unsigned below = lanemask_lt();
-    for (int j0 = 0; j0 < n; j0 += nt) {
-        const int j = j0 + tid;
-        const unsigned long long v = j < n ? ck(j) : 0ull;
-        const bool in = v >= T && v != 0ull;
-        const unsigned mask = __ballot_sync(0xffffffffu, in);
-        int base = 0;
-        if (lane == 0 && mask) base = atomicAdd(&s.ncand, __popc(mask));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const int pos = base + __popc(mask & below);
-        if (in && pos < kCap) cand[pos] = v;
-    }
-    __syncthreads();
-    const int nc = s.ncand;
-    if (nc > kCap) return false;
-    for (int c = tid; c < nc; c += nt) {
-        const unsigned long long v = cand[c];
-        int rank = 0;
-        for (int c2 = 0; c2 < nc; ++c2) rank += cand[c2] > v;
-        if (rank < want) flags[0xffffffffu - static_cast<uint32_t>(v & 0xffffffffu)] |= kPick;
-    }
-    __syncthreads();
-    return true;
 }
 
 // One warp writes the indices j with (flags[j] & bits) in ascending order
