@@ -18,9 +18,10 @@
 // unit of 2..8 chunks runs as a thread-block cluster whose CTAs write their
 // probe scores and importance sums into the leader CTA's shared memory
 // (larger units use global buffers and an arrival counter).  The leader then
-// selects for each query head: histogram top-k passes for the importance
-// picks and the probe fill, a min-reduction for the recency eviction, and the
-// indices written in ascending order.
+// selects: the importance picks, then every query head at once, one warp
+// each (up to 256 blocks: max-extraction rounds on the warp's registers; more
+// blocks: histogram top-k passes over the CTA), a min-reduction for the
+// recency eviction, and the indices written in ascending order.
 #include <cooperative_groups.h>
 
 #include "qs_internal.cuh"
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     static_assert(kLanesPerRow >= 1 && kLanesPerRow <= 32, "row must span 1..32 lanes");
 
     // dynamic: probe keys [G][MKBPR] u32, importance keys [MKBPR] u32,
-    // flags [MKBPR] u8, importance flags [MKBPR] u8
+    // flags [G][MKBPR] u8, importance flags [MKBPR] u8
     extern __shared__ __align__(16) uint8_t dyn[];
     __shared__ __align__(16) float s_q[G][D];
     __shared__ __align__(16) int8_t s_q8[G][D];
@@ -136,8 +137,8 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     const int n_probe = max(1, a.n_probe);
     uint32_t* pkeys = reinterpret_cast<uint32_t*>(dyn);
     uint32_t* ikeys = pkeys + static_cast<size_t>(G) * a.MKBPR;
-    uint8_t* flags = reinterpret_cast<uint8_t*>(ikeys + a.MKBPR);
-    uint8_t* imp_flags = flags + a.MKBPR;
+    uint8_t* flags = reinterpret_cast<uint8_t*>(ikeys + a.MKBPR);   // [G][MKBPR]
+    uint8_t* imp_flags = flags + static_cast<size_t>(G) * a.MKBPR;
     uint32_t* dst_pkeys = pkeys;
     uint32_t* dst_ikeys = ikeys;
     if constexpr (MODE == kCluster) {
@@ -336,12 +337,58 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
 
     // ---- importance pre-selection (same for every head of the request)
     const int n_imp = a.importance ? min((a.k + 1) / 2, nb) : 0;
+    const bool small = nb <= kWarpSmallMax && G <= kThreads / 32;
     for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = kCand;
     __syncthreads();
-    if (n_imp > 0) topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
+    if (n_imp > 0) {
+        if (small) {
+            if (warp == 0) warp_topk_small(ikeys, imp_flags, nb, n_imp);
+            __syncthreads();
+        } else {
+            topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
+        }
+    }
     for (int j = threadIdx.x; j < nb; j += kThreads)
         imp_flags[j] = (imp_flags[j] & kPick) ? kFixed : 0;
     const int want = min(a.k - n_imp, nb - n_imp);
+    if (small) {
+        // one warp per query head, no block barrier: probe fill, recency,
+        // ordered output
+        __syncthreads();
+        if (warp < G) {
+            const int h = warp;
+            const size_t row = static_cast<size_t>(b) * a.H + n * G + h;
+            const uint32_t* keys = pkeys + static_cast<size_t>(h) * a.MKBPR;
+            uint8_t* fl = flags + static_cast<size_t>(h) * a.MKBPR;
+            for (int j = lane; j < nb; j += 32) fl[j] = imp_flags[j] ? kFixed : kCand;
+            __syncwarp();
+            warp_topk_small(keys, fl, nb, want);
+            if (want > 0 && !(fl[nb - 1] & (kFixed | kPick))) {
+                // the last block replaces the probe pick with the lowest probe
+                // score (ties: the larger index); importance picks stay
+                unsigned long long mine = ~0ull;
+                for (int j = lane; j < nb; j += 32)
+                    if (fl[j] & kPick) {
+                        const unsigned long long c = (static_cast<unsigned long long>(keys[j]) << 32) |
+                                                     (0xffffffffu - static_cast<uint32_t>(j));
+                        mine = c < mine ? c : mine;
+                    }
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const unsigned long long other = __shfl_xor_sync(0xffffffffu, mine, o);
+                    mine = other < mine ? other : mine;
+                }
+                if (lane == 0) {
+                    const int victim = static_cast<int>(0xffffffffu - static_cast<uint32_t>(mine & 0xffffffffu));
+                    fl[victim] &= static_cast<uint8_t>(~kPick);
+                    fl[nb - 1] |= kPick;
+                }
+                __syncwarp();
+            }
+            warp_emit_flags(fl, kFixed | kPick, nb, a.k, a.selected + row * a.k);
+        }
+        return;
+    }
 
     // ---- per query head: probe fill, recency insurance, ordered output
     for (int h = 0; h < G; ++h) {
@@ -406,7 +453,7 @@ qs_status launch_mode(const ProbeArgs& a, int chunks, size_t smem, cudaStream_t 
 
 template <Dt KT, int D, int G>
 qs_status launch(const ProbeArgs& a, cudaStream_t s) {
-    const size_t smem = align_up(static_cast<size_t>(a.MKBPR) * (4 * G + 4 + 2), 16);
+    const size_t smem = align_up(static_cast<size_t>(a.MKBPR) * (4 * G + 4 + G + 1), 16);
     if (smem > 160 * 1024) return QS_EUNSUPPORTED;
     constexpr int kBlocksPerChunk = blocks_per_chunk<KT, D>();
     const int chunks = max(1, (a.MKBPR + kBlocksPerChunk - 1) / kBlocksPerChunk);

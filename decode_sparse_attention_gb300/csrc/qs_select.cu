@@ -167,6 +167,10 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
 
 // Forced set, top-k and emission of one unit whose nb keys are in keys_s
 // (step 2.3 + window).  All threads; ends with a barrier.
+// kWarpPath: units of up to kWarpSmallMax blocks select with the one-warp
+// max-extraction top-k (measured faster in the one-CTA-per-unit selector; in
+// the top-k kernel after the scan the histogram levels alone measured faster).
+template <bool kWarpPath>
 QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, const uint32_t* keys_s,
                            uint8_t* flags, int32_t* sel_out, TopkFastScratch& s_fast,
                            TopkScratch<kThreads>& s_topk) {
@@ -178,13 +182,22 @@ QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, const uint32_t* k
         __syncthreads();
         return;
     }
-    topk_fast_clear<kThreads>(s_fast, nb);
+    const bool small = kWarpPath && nb <= kWarpSmallMax;
+    if (!small) topk_fast_clear<kThreads>(s_fast, nb);
     for (int j = threadIdx.x; j < nb; j += kThreads)
         flags[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
     __syncthreads();
     const int want = min(a.k - n_forced, nb - n_forced);
-    topk_fast<kThreads>(keys_s, flags, nb, want, s_fast, s_topk);
-    block_emit_flags<kThreads>(flags, kFixed | kPick, nb, a.k, sel_out, s_topk);
+    if (small) {
+        // one warp: max-extraction rounds, then the ordered output
+        if (threadIdx.x < 32) {
+            warp_topk_small(keys_s, flags, nb, want);
+            warp_emit_flags(flags, kFixed | kPick, nb, a.k, sel_out);
+        }
+    } else {
+        topk_fast<kThreads>(keys_s, flags, nb, want, s_fast, s_topk);
+        block_emit_flags<kThreads>(flags, kFixed | kPick, nb, a.k, sel_out, s_topk);
+    }
     __syncthreads();
 }
 
@@ -211,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2) quest_select_unit_kernel(SelectAr
     score_chunk<MT, D>(a, b, n, 0, nb, keys,
                        a.scores_out ? a.scores + static_cast<size_t>(u) * maxnb : nullptr);
     __syncthreads();
-    select_unit(a, L, nb, keys, flags, sel_out, s_fast, s_topk);
+    select_unit<true>(a, L, nb, keys, flags, sel_out, s_fast, s_topk);
 }
 
 // ---- units longer than one chunk: a streaming scan, then one top-k per unit
@@ -453,7 +466,7 @@ __global__ void __launch_bounds__(kThreads) quest_unit_topk_kernel(SelectArgs a)
     const float* scores_u = a.scores + static_cast<size_t>(u) * maxnb;
     for (int j = threadIdx.x; j < nb; j += kThreads) keys[j] = float_key(ldcg_f32(scores_u + j));
     __syncthreads();
-    select_unit(a, L, nb, keys, flags, sel_out, s_fast, s_topk);
+    select_unit<false>(a, L, nb, keys, flags, sel_out, s_fast, s_topk);
 }
 
 template <Dt MT, int D>
