@@ -14,9 +14,15 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libquestsparse.so")
 OBJDIR = os.path.join(HERE, "_build")
-SOURCES = ["qs_api.cu", "qs_metadata.cu", "qs_select.cu", "qs_probe.cu", "qs_attention.cu",
-           "qs_importance.cu",
-           "qs_attention_noalloc.cu", "qs_step_fused.cu"]
+# (source, object name, defines): qs_probe.cu compiles once for its host
+# part and once per (KV dtype, head size) pair of kernel variants
+PROBE_VARIANTS = [("F32", 128), ("F32", 64), ("BF16", 128), ("BF16", 64), ("F16", 128),
+                  ("F16", 64), ("I8", 128)]
+SOURCES = ([(f, os.path.splitext(f)[0], []) for f in
+            ["qs_api.cu", "qs_metadata.cu", "qs_select.cu", "qs_probe.cu", "qs_attention.cu",
+             "qs_importance.cu", "qs_attention_noalloc.cu", "qs_step_fused.cu"]] +
+           [("qs_probe.cu", "qs_probe_%s_%d" % (t, d), ["-DQS_PROBE_KT=%s" % t, "-DQS_PROBE_D=%d" % d])
+            for t, d in PROBE_VARIANTS])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]
@@ -33,9 +39,10 @@ def _inputs():
     return deps
 
 
-def _compile(src, verbose):
-    obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c",
+def _compile(job, verbose):
+    src, name, defines = job
+    obj = os.path.join(OBJDIR, name + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *defines, "-I", os.path.join(ROOT, "include"), "-c",
            os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
@@ -50,7 +57,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
         return LIB
     os.makedirs(OBJDIR, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), max(4, os.cpu_count() or 4))) as ex:
         results = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
     if verbose:
         for _, log in results:

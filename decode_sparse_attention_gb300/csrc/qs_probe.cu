@@ -28,10 +28,6 @@
 #include "qs_topk.cuh"
 
 namespace qs {
-namespace {
-
-constexpr int kThreads = 256;
-constexpr int kMaxG = 8;
 
 struct ProbeArgs {
     const void* q;
@@ -51,6 +47,14 @@ struct ProbeArgs {
     uint32_t* counters;    // [B*N]
     int32_t* dev_status;
 };
+
+// Launches the selector for one KV dtype and head size; G = H/N in {1,2,4,8}.
+template <Dt KT, int D> qs_status probe_launch(const ProbeArgs& a, int G, cudaStream_t s);
+
+#if defined(QS_PROBE_KT)
+namespace {
+
+constexpr int kThreads = 256;
 
 // q . K-row partial over one 16-byte chunk, for G heads.
 template <Dt T, int G> struct ProbeChunk;
@@ -462,8 +466,10 @@ qs_status launch(const ProbeArgs& a, cudaStream_t s) {
     return launch_mode<KT, D, G, kGlobal>(a, chunks, smem, s);
 }
 
+}  // namespace
+
 template <Dt KT, int D>
-qs_status launch_g(const ProbeArgs& a, int G, cudaStream_t s) {
+qs_status probe_launch(const ProbeArgs& a, int G, cudaStream_t s) {
     switch (G) {
         case 1: return launch<KT, D, 1>(a, s);
         case 2: return launch<KT, D, 2>(a, s);
@@ -473,6 +479,24 @@ qs_status launch_g(const ProbeArgs& a, int G, cudaStream_t s) {
     }
 }
 
+// One (KV dtype, D) pair per object file: the build compiles this file once
+// per pair so that the kernel variants compile in parallel.
+template qs_status probe_launch<Dt::QS_PROBE_KT, QS_PROBE_D>(const ProbeArgs&, int, cudaStream_t);
+
+}  // namespace qs
+#endif  // QS_PROBE_KT
+
+#if !defined(QS_PROBE_KT)
+extern template qs_status probe_launch<Dt::F32, 128>(const ProbeArgs&, int, cudaStream_t);
+extern template qs_status probe_launch<Dt::F32, 64>(const ProbeArgs&, int, cudaStream_t);
+extern template qs_status probe_launch<Dt::BF16, 128>(const ProbeArgs&, int, cudaStream_t);
+extern template qs_status probe_launch<Dt::BF16, 64>(const ProbeArgs&, int, cudaStream_t);
+extern template qs_status probe_launch<Dt::F16, 128>(const ProbeArgs&, int, cudaStream_t);
+extern template qs_status probe_launch<Dt::F16, 64>(const ProbeArgs&, int, cudaStream_t);
+extern template qs_status probe_launch<Dt::I8, 128>(const ProbeArgs&, int, cudaStream_t);
+
+namespace {
+constexpr int kMaxG = 8;
 }  // namespace
 
 size_t probe_workspace_bytes(int B, int H, int N, int MKBPR) {
@@ -524,10 +548,10 @@ qs_status probe_select_impl(const void* q, qs_dtype q_dtype, const void* k_cache
                                              align_up(static_cast<size_t>(B) * N * MKBPR * 4, 256));
     a.dev_status = dev_status;
     switch (kv_dtype) {
-        case QS_F32: return D == 128 ? launch_g<Dt::F32, 128>(a, G, stream) : launch_g<Dt::F32, 64>(a, G, stream);
-        case QS_BF16: return D == 128 ? launch_g<Dt::BF16, 128>(a, G, stream) : launch_g<Dt::BF16, 64>(a, G, stream);
-        case QS_F16: return D == 128 ? launch_g<Dt::F16, 128>(a, G, stream) : launch_g<Dt::F16, 64>(a, G, stream);
-        case QS_I8: return launch_g<Dt::I8, 128>(a, G, stream);
+        case QS_F32: return D == 128 ? probe_launch<Dt::F32, 128>(a, G, stream) : probe_launch<Dt::F32, 64>(a, G, stream);
+        case QS_BF16: return D == 128 ? probe_launch<Dt::BF16, 128>(a, G, stream) : probe_launch<Dt::BF16, 64>(a, G, stream);
+        case QS_F16: return D == 128 ? probe_launch<Dt::F16, 128>(a, G, stream) : probe_launch<Dt::F16, 64>(a, G, stream);
+        case QS_I8: return probe_launch<Dt::I8, 128>(a, G, stream);
         default: return QS_EDTYPE;
     }
 }
@@ -548,3 +572,4 @@ extern "C" qs_status qs_probe_select(const void* q, qs_dtype q_dtype, const void
                                  H, N, D, BS, k, n_probe, selected, workspace, workspace_bytes,
                                  dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
+#endif  // !QS_PROBE_KT
