@@ -10,12 +10,16 @@ tokens, the largest configuration) gives the contract keys (value, roofline,
 e2e, cpu_baseline, clocks, gpu_launches); every workload of --configs is then
 measured the same way and reported as its own record under "configs".
 
-Timing: the step is captured as a CUDA graph for each of R input sets
-(same shapes and lengths, other seeds), R chosen so that one rotation moves
-more than 3x the 129 MB L2; W warm-up steps, then K steps replayed back to
-back in rotation, each set's inputs evicted from L2 by the others' traffic
-before its next turn.  value = the span of the K steps on the launching
-stream's CUDA events / K.  Workloads too small for a rotation of at most
+Timing: the step runs once for each of R input sets (same shapes and
+lengths, other seeds), R chosen so that one rotation moves more than 3x the
+129 MB L2, and the R steps are captured back to back in one CUDA graph, as
+consecutive layers of one forward graph would run them; W warm-up steps,
+then K steps (whole rotations, then single-step graphs for the remainder)
+replayed back to back, each set's inputs evicted from L2 by the others'
+traffic before its next turn.  value = the span of the K steps on the
+launching stream's CUDA events / K.  The same loop with one graph per step
+(which adds the graph-to-graph launch gap to every step) is reported beside
+it.  Workloads too small for a rotation of at most
 --max-sets sets are timed one step at a time with a 256 MiB L2 flush before
 each.  The dominant kernel (the attention) and the selector are timed alone
 the same way; a flushed one-step time is reported beside the value.  Under
@@ -390,6 +394,37 @@ def timed_rotation(graphs, steps, stream):
     return iv, evs[0].elapsed_time(evs[-1])
 
 
+def capture_rotation(fns, stream):
+    """One CUDA graph holding one call of each fn, back to back on one stream
+    (each fn was already run once eagerly by capture())."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in fns:
+            fn()
+    return g
+
+
+def timed_rotation_graph(g_rot, singles, steps, stream):
+    """Exactly `steps` steps: the rotation graph (one step per input set)
+    replayed back to back, then single-step graphs for the remainder.
+    Returns per-step times (ms) of each rotation (its interval / R) and the
+    whole span (ms) from the first event to the last."""
+    R = len(singles)
+    full, rest = divmod(steps, R)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(full + 2)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(full):
+            g_rot.replay()
+            evs[i + 1].record(stream)
+        for i in range(rest):
+            singles[i].replay()
+        evs[-1].record(stream)
+    torch.cuda.synchronize()
+    iv = [evs[i].elapsed_time(evs[i + 1]) / R for i in range(full)]
+    return iv, evs[0].elapsed_time(evs[-1])
+
+
 def l2_bytes(dev):
     try:
         return int(torch.cuda.get_device_properties(dev).L2_cache_size)
@@ -480,9 +515,11 @@ def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
 
     # graphs: the step, the selector alone and the attention alone per set
     g_step, g_sel, g_attn = [], [], []
+    f_step, f_sel, f_attn = [], [], []
     keep = []   # buffers the captured graphs write into must outlive them
     for (x, _, sel, out, params, _) in sets:
-        g_step.append(capture(lambda params=params: qs.sparse_decode_step(params, dev), stream))
+        f_step.append(lambda params=params: qs.sparse_decode_step(params, dev))
+        g_step.append(capture(f_step[-1], stream))
         sel2 = torch.empty_like(sel)
 
         def run_selector(x=x, sel2=sel2):
@@ -494,6 +531,7 @@ def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
                 qs.probe_select(x["q"], x["k_cache"], x["block_tables"], x["seq_lens"], w.k,
                                 w.n_probe, importance=x.get("importance"),
                                 k_scale=x.get("k_scale"), selected=sel2)
+        f_sel.append(run_selector)
         g_sel.append(capture(run_selector, stream))
         attn_out = torch.empty_like(out)
 
@@ -501,8 +539,16 @@ def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
             qs.sparse_decode_attn(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
                                   x["seq_lens"], sel, k_scale=x.get("k_scale"),
                                   v_scale=x.get("v_scale"), out=attn_out)
+        f_attn.append(run_attn)
         g_attn.append(capture(run_attn, stream))
         keep.append((sel2, attn_out))
+    # the R steps (and the kernels alone) of one rotation back to back in one
+    # graph, as consecutive layers of one forward graph would run them
+    r_step = r_sel = r_attn = None
+    if rotate:
+        r_step = capture_rotation(f_step, stream)
+        r_sel = capture_rotation(f_sel, stream)
+        r_attn = capture_rotation(f_attn, stream)
     torch.cuda.synchronize()
     # algorithmic bytes: the mean over the sets (selections differ per set)
     per_set = [step_bytes(w, s[0], s[2].cpu().numpy(), q_es) for s in sets]
@@ -521,16 +567,19 @@ def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
     torch.cuda.synchronize()
     barrier()
     if rotate:
-        durs, span = timed_rotation(g_step, args.steps, stream)
+        durs, span = timed_rotation_graph(r_step, g_step, args.steps, stream)
         step_us = 1000.0 * span / args.steps
+        _, span1 = timed_rotation(g_step, args.steps, stream)
+        step_us_graph_per_step = 1000.0 * span1 / args.steps
     else:
         durs = timed_graph(g_step[0], flush, sink, args.steps, stream)
         step_us = 1000.0 * sum(durs) / len(durs)
+        step_us_graph_per_step = step_us
     barrier()
     n_side = max(args.steps // 2, 3)
     if rotate:
-        _, attn_span = timed_rotation(g_attn, n_side, stream)
-        _, sel_span = timed_rotation(g_sel, n_side, stream)
+        _, attn_span = timed_rotation_graph(r_attn, g_attn, n_side, stream)
+        _, sel_span = timed_rotation_graph(r_sel, g_sel, n_side, stream)
         attn_us = 1000.0 * attn_span / n_side
         sel_us = 1000.0 * sel_span / n_side
     else:
@@ -582,9 +631,13 @@ def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
                    "rotation, %.0f MB of step traffic per rotation vs %d MB of L2"
                    % (len(sets), len(sets) * nbytes["step"] / 1e6, l2_bytes(dev) >> 20))
                   if rotate else "256 MiB written then read back between timed steps",
-            "step": "qs_sparse_decode_step captured as one CUDA graph per input set; "
-                    + ("graphs replayed back to back, value = span / steps" if rotate
-                       else "value = mean of per-step event pairs"),
+            "step": ("qs_sparse_decode_step once per input set, the R steps of a rotation "
+                     "captured back to back in one CUDA graph (as consecutive layers of one "
+                     "forward graph run); the graph replayed back to back, value = span / "
+                     "steps; step_us_graph_per_step: one graph per step instead"
+                     if rotate else
+                     "qs_sparse_decode_step captured as one CUDA graph; value = mean of "
+                     "per-step event pairs"),
             "fused_select": args.fused_select,
             "kernels_per_step": kernels,
         },
@@ -596,6 +649,7 @@ def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
         "step_frac_of_8tbs": round(nbytes["step"] / (step_us_max * 1e-6) / 1e9 / 8000.0, 4),
         "algorithmic_bytes": nbytes,
         "step_us_p10_p50_p90": [round(1000 * float(np.percentile(durs, p)), 3) for p in (10, 50, 90)],
+        "step_us_graph_per_step": round(step_us_graph_per_step, 3),
         "step_us_flushed_single": round(1000.0 * statistics.median(flushed), 3),
         "roofline": {
             "kernel": "sparse_attn_kernel",
@@ -642,7 +696,7 @@ def measure(args, w, dev, stream, flush, sink, rank, cpu_seconds, headline):
                                       % upd_bytes)
     if rank == 0 and cpu_seconds > 0:
         rec["cpu_baseline"] = cpu_baseline(w, x0, cpu_seconds)
-    del sets, keep, g_step, g_sel, g_attn
+    del sets, keep, g_step, g_sel, g_attn, r_step, r_sel, r_attn, f_step, f_sel, f_attn
     return rec
 
 
@@ -842,7 +896,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-importance", action="store_true",
                     help="skip timing the prefill importance producer")
-    ap.add_argument("--max-sets", type=int, default=32,
+    ap.add_argument("--max-sets", type=int, default=128,
                     help="most input sets to rotate through; workloads needing more (tiny "
                          "steps) are timed with an L2 flush between steps instead")
     ap.add_argument("--fused-select", type=int, default=-1, choices=[-1, 0, 1],

@@ -28,14 +28,15 @@
 //    combines its output channels).  Q.K uses 8 lanes per token and packed
 //    fp32x2 FMAs with a transposing shuffle reduction; P.V gives each lane
 //    D/32 output channels and runs over all of a warp's rows (p = 0 past the
-//    valid ones; the ring is zeroed once per launch so those bytes are
-//    finite); the accumulators are rescaled only when a head's max grew.
+//    valid ones: when a warp loads fewer than its rows of a tile it zeroes
+//    the V rows, and int8 scales, it leaves out, so those bytes are finite);
+//    the accumulators are rescaled only when a head's max grew.
 //  * A unit split across CTAs is merged on the device: each CTA writes a
 //    (max, sum, acc) partial; the last to arrive (atomic counter, no spin)
 //    combines them and rearms the counter.
 //  * Inside the decode step it is launched as a programmatic dependent of the
 //    selector: the staging copies (none of which read what the selector
-//    writes) and the ring zeroing happen before the grid-dependency wait.
+//    writes) are issued before the grid-dependency wait.
 #pragma once
 
 #include <cmath>
@@ -54,6 +55,7 @@ constexpr int kMaxTilesPerCta = 512;
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 225 * 1024;
 constexpr size_t kStageTablesMax = 64 * 1024;   // block-table rows staged in shared memory
+constexpr int kMergeFast = 8;            // split partials merged in one round trip
 
 struct AttnArgs {
     const uint8_t* q;
@@ -441,18 +443,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
     // ---- prologue: stage what the preceding kernel does not write (query
     // rows, block-table rows, lengths; fused: metadata-table rows), then wait
     // for it (the selection), then convert the queries and build the tile list
-    // ring bytes are zeroed once, so that the rows a warp never loads hold
-    // finite values: P.V runs over all of a warp's rows with p = 0 past the
-    // valid ones (the staging area at the ring's start is zeroed after use)
-    const size_t ring_bytes = static_cast<size_t>(a.NW) * S * a.stage_bytes;
-    auto zero_ring = [&](size_t lo, size_t hi) {
-        for (size_t o = lo + static_cast<size_t>(tid) * 16; o < hi; o += static_cast<size_t>(nthreads) * 16)
-            *reinterpret_cast<uint4*>(stages + o) = make_uint4(0, 0, 0, 0);
-    };
     stage_unit_inputs<D, G>(a, u_first, n_units, b_first, n_req, stages);
     if constexpr (kSel) stage_meta_tables(a, u_first, n_units, stages);
     cp_async_commit();
-    zero_ring(a.sel_end, ring_bytes);
     if constexpr (!kSel) pdl_wait();   // the selection is written by the preceding kernel
     cp_async_wait(0);
     __syncthreads();
@@ -511,8 +504,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
         info[i] = ti;
     }
     __syncthreads();   // the staging area is free from here on: the ring takes it
-    zero_ring(0, a.sel_end);
-    __syncthreads();
 
     // ---- per-warp row streams: lane -> (row within a copy step, 16-byte
     // chunk) of the warp's kRPW rows, offsets fixed for the whole loop
@@ -545,23 +536,35 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
                         cp_async16_s(d + vpart + j * dstep, vs + j * jstep);
                     }
                 } else {
+                    // rows past rw: P.V reads them with p = 0, so their V
+                    // bytes are zeroed (the slot may never have been loaded)
 #pragma unroll
                     for (int j = 0; j < kCopies; ++j)
                         if (c_row + j * kRowsPerCopy < rw) {
                             cp_async16_s(d + j * dstep, ks + j * jstep);
                             cp_async16_s(d + vpart + j * dstep, vs + j * jstep);
+                        } else {
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(d + vpart + j * dstep),
+                                         "r"(0u)
+                                         : "memory");
                         }
                 }
                 if constexpr (kInt8) {
-                    // one fp32 scale per (token, KV head): index off / ROWB
-                    if (lane < min(rw, kRPW)) {
-                        const size_t si = static_cast<size_t>(ti.off / ROWB) +
-                                          static_cast<size_t>(r0 + lane) * a.N;
+                    // one fp32 scale per (token, KV head): index off / ROWB;
+                    // zero past rw (P.V multiplies p = 0 by the V scale)
+                    if (lane < kRPW) {
                         const uint32_t sd = smem_addr(stages) +
                                             static_cast<uint32_t>(warp * S + st) * a.stage_bytes +
                                             2 * a.rows_bytes + lane * 4;
-                        cp_async4_s(sd, a.ks + si);
-                        cp_async4_s(sd + kRPW * 4, a.vs + si);
+                        if (lane < rw) {
+                            const size_t si = static_cast<size_t>(ti.off / ROWB) +
+                                              static_cast<size_t>(r0 + lane) * a.N;
+                            cp_async4_s(sd, a.ks + si);
+                            cp_async4_s(sd + kRPW * 4, a.vs + si);
+                        } else {
+                            asm volatile("st.shared.u32 [%0], %1;" ::"r"(sd), "r"(0u) : "memory");
+                            asm volatile("st.shared.u32 [%0], %1;" ::"r"(sd + kRPW * 4), "r"(0u) : "memory");
+                        }
                     }
                 }
             }
@@ -892,11 +895,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
             for (int idx = tid; idx < G * D; idx += nthreads) {
                 const int h = idx / D, d = idx % D;
                 float M = -INFINITY, Ls = 0.f, A = 0.f;
-                if (ncta <= 4) {
+                if (ncta <= kMergeFast) {
                     // the usual case: every partial requested in one round trip
-                    float mv[4], lv[4], av[4];
+                    float mv[kMergeFast], lv[kMergeFast], av[kMergeFast];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < kMergeFast; ++q) {
                         mv[q] = -INFINITY;
                         lv[q] = av[q] = 0.f;
                         if (q < ncta) {
@@ -907,10 +910,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) sparse_attn_kernel(const At
                         }
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) M = fmaxf(M, mv[q]);
+                    for (int q = 0; q < kMergeFast; ++q) M = fmaxf(M, mv[q]);
                     if (M != -INFINITY) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
+                        for (int q = 0; q < kMergeFast; ++q) {
                             const float f = q < ncta ? exp2_approx(mv[q] - M) : 0.f;
                             Ls += lv[q] * f;
                             A += av[q] * f;

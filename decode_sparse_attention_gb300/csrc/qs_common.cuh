@@ -92,6 +92,48 @@ QS_DEVINL void stg_v4(void* p, uint4 v) {
                  : "memory");
 }
 
+// Loads issued exactly where they stand (asm volatile: the compiler may not
+// sink them below a branch on an earlier load), so that round trips that do
+// not depend on one another overlap.  Read-only data only.
+QS_DEVINL int32_t ldg_now_s32(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+QS_DEVINL uint32_t ldg_now_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+QS_DEVINL uint32_t ldg_now_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+QS_DEVINL uint2 ldg_now_v2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+QS_DEVINL uint4 ldg_now_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+// Raw bits of q element i (fp32: the word; 16-bit: the half-word) and their
+// value; split so that the load is issued before a branch and converted after.
+QS_DEVINL uint32_t ldg_now_q_bits(const void* q, int dt, size_t i) {
+    return dt == QS_F32 ? ldg_now_u32(static_cast<const float*>(q) + i)
+                        : ldg_now_u16(static_cast<const uint16_t*>(q) + i);
+}
+QS_DEVINL float q_bits_value(uint32_t w, int dt) {
+    if (dt == QS_F32) return __uint_as_float(w);
+    if (dt == QS_BF16) return __uint_as_float(w << 16);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w)));
+}
+
 // L2-coherent loads for data written by other CTAs of the same grid.
 QS_DEVINL float ldcg_f32(const float* p) { return __ldcg(p); }
 

@@ -12,16 +12,18 @@
 //
 // GB300 design: grid = (block chunks, B*N).  A CTA scores a chunk of blocks
 // for all H/N query heads of one KV head, so each probed K row is read once
-// for the whole group; every lane group has all probe rows of its two blocks
-// in flight at once, and while they are, its warps sum the prefill
-// importance of the chunk's blocks (one warp per block, in token order).  A
-// unit of 2..8 chunks runs as a thread-block cluster whose CTAs write their
-// probe scores and importance sums into the leader CTA's shared memory
-// (larger units use global buffers and an arrival counter).  The leader then
-// selects: the importance picks, then every query head at once, one warp
-// each (up to 256 blocks: max-extraction rounds on the warp's registers; more
-// blocks: histogram top-k passes over the CTA), a min-reduction for the
-// recency eviction, and the indices written in ascending order.
+// for the whole group.  The request's length, the chunk's block-table
+// entries, the queries and the chunk's prefill importance (into L2) are all
+// requested in one round trip; every lane group then has all probe rows of
+// its two blocks in flight at once, and while they are, one thread per block
+// sums the block's importance in token order.  A unit of 2..8 chunks runs as
+// a thread-block cluster whose CTAs write their probe scores and importance
+// sums into the leader CTA's shared memory (larger units use global buffers
+// and an arrival counter).  The leader then selects: the importance picks,
+// then every query head at once (up to 256 blocks: counting top-k over all
+// heads with every thread; more blocks: histogram top-k passes over the CTA,
+// one head at a time), a min-reduction for the recency eviction, and the
+// indices written in ascending order.
 #include <cooperative_groups.h>
 
 #include "qs_internal.cuh"
@@ -99,7 +101,7 @@ template <Dt KT, int D> constexpr int blocks_per_chunk() {
 constexpr int kProbeBatch = 8;     // probe rows of one block loaded together
 
 template <Dt KT, int D, int G, int MODE>
-__global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) probe_select_kernel(ProbeArgs a) {
     constexpr bool kInt8 = KT == Dt::I8;
     constexpr int kElemBytes = DtInfo<KT>::bytes;
     constexpr int kLanesPerRow = D * kElemBytes / 16;
@@ -108,8 +110,9 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     constexpr int kBlocksPerChunk = blocks_per_chunk<KT, D>();
     static_assert(kLanesPerRow >= 1 && kLanesPerRow <= 32, "row must span 1..32 lanes");
 
-    // dynamic: probe keys [G][MKBPR] u32, importance keys [MKBPR] u32,
-    // flags [G][MKBPR] u8, importance flags [MKBPR] u8
+    // dynamic: probe keys [G][kstr] u32, importance keys [kstr] u32 (kstr =
+    // MKBPR rounded up to 4 words), flags [G][MKBPR] u8, importance flags
+    // [MKBPR] u8
     extern __shared__ __align__(16) uint8_t dyn[];
     __shared__ __align__(16) float s_q[G][D];
     __shared__ __align__(16) int8_t s_q8[G][D];
@@ -124,7 +127,35 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     const int u = blockIdx.y;
     const int b = u / a.N, n = u % a.N;
     const int BS = a.BS;
-    const int L = a.seq_lens[b];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int grp = threadIdx.x / kLanesPerRow;
+    const int cl = threadIdx.x % kLanesPerRow;
+    const int j_base = blockIdx.x * kBlocksPerChunk + grp;
+    const int kstr = (a.MKBPR + 3) & ~3;
+    // one round trip for everything that depends on no other load: the
+    // length, the lane group's block-table entries, the queries and (into
+    // L2) the importance of the chunk's tokens
+    const int L = ldg_now_s32(a.seq_lens + b);
+    int p_raw[2];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int j = j_base + jj * kGroups;
+        p_raw[jj] = j < a.MKBPR ? ldg_now_s32(a.bt + static_cast<size_t>(b) * a.MKBPR + j) : -1;
+    }
+    constexpr int kQPerThread = (G * D + kThreads - 1) / kThreads;
+    uint32_t qbits[kQPerThread];
+#pragma unroll
+    for (int r = 0; r < kQPerThread; ++r) {
+        const int i = threadIdx.x + r * kThreads;
+        qbits[r] = i < G * D ? ldg_now_q_bits(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + n * G) * D + i) : 0u;
+    }
+    const float* imp_row = a.importance ? a.importance + static_cast<size_t>(b) * a.imp_stride : nullptr;
+    if (imp_row) {
+        const long long t0 = static_cast<long long>(blockIdx.x) * kBlocksPerChunk * BS;
+        const long long t1 = min(static_cast<long long>(a.imp_stride), t0 + static_cast<long long>(kBlocksPerChunk) * BS);
+        for (long long t = t0 + static_cast<long long>(threadIdx.x) * 32; t < t1; t += kThreads * 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(imp_row + t));
+    }
     const bool bad_len = L < 0 || L > a.MKBPR * BS ||
                          (a.importance != nullptr && L > a.imp_stride);
     if (bad_len) {   // uniform over the unit's CTAs
@@ -140,8 +171,8 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     if (MODE != kCluster && static_cast<int>(blockIdx.x) >= n_chunks) return;
     const int n_probe = max(1, a.n_probe);
     uint32_t* pkeys = reinterpret_cast<uint32_t*>(dyn);
-    uint32_t* ikeys = pkeys + static_cast<size_t>(G) * a.MKBPR;
-    uint8_t* flags = reinterpret_cast<uint8_t*>(ikeys + a.MKBPR);   // [G][MKBPR]
+    uint32_t* ikeys = pkeys + static_cast<size_t>(G) * kstr;
+    uint8_t* flags = reinterpret_cast<uint8_t*>(ikeys + kstr);   // [G][MKBPR]
     uint8_t* imp_flags = flags + static_cast<size_t>(G) * a.MKBPR;
     uint32_t* dst_pkeys = pkeys;
     uint32_t* dst_ikeys = ikeys;
@@ -152,12 +183,12 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     topk_fast_clear<kThreads>(s_fast, nb);
 
     // queries of the group (fp32), plus the int8 quantisation for int8 caches
-    for (int i = threadIdx.x; i < G * D; i += kThreads) {
-        const int h = i / D, d = i % D;
-        s_q[h][d] = load_q(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + n * G + h) * D + d);
+#pragma unroll
+    for (int r = 0; r < kQPerThread; ++r) {
+        const int i = threadIdx.x + r * kThreads;
+        if (i < G * D) s_q[i / D][i % D] = q_bits_value(qbits[r], a.q_dt);
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if constexpr (kInt8) {
         for (int h = warp; h < G; h += kThreads / 32) {
             float amax = 0.f;
@@ -176,8 +207,6 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     }
 
     // ---- probe scores of this chunk's blocks (two blocks per lane group)
-    const int grp = threadIdx.x / kLanesPerRow;
-    const int cl = threadIdx.x % kLanesPerRow;
     const unsigned gmask = kLanesPerRow == 32
                                ? 0xffffffffu
                                : (((1u << kLanesPerRow) - 1u) << (lane / kLanesPerRow * kLanesPerRow));
@@ -195,7 +224,6 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         }
     }
     const size_t row_bytes = static_cast<size_t>(a.N) * D * kElemBytes;
-    const int j_base = blockIdx.x * kBlocksPerChunk + grp;
     int p_blk[2], p0s[2], steps[2], nps[2];
     uint4 v[2][kProbeBatch];
     float sk[2][kProbeBatch];
@@ -205,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         nps[jj] = 0;
         p_blk[jj] = -1;
         if (j < nb) {
-            const int p = a.bt[static_cast<size_t>(b) * a.MKBPR + j];
+            const int p = p_raw[jj];
             if (p < 0 || p >= a.num_kv_blocks) {
                 if (cl == 0) set_status(a.dev_status, QS_DEV_EBLOCK_TABLE);
             } else {
@@ -234,24 +262,24 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         }
     }
     // importance of this chunk's blocks while the probe rows are in flight:
-    // one warp per block, coalesced loads, the sum taken in token order (fp32,
-    // sequential, as the importance picks require)
-    if (a.importance) {
-        const float* imp = a.importance + static_cast<size_t>(b) * a.imp_stride;
-        for (int jj = warp; jj < kBlocksPerChunk; jj += kThreads / 32) {
+    // one thread per block, the sum taken in token order (fp32, sequential,
+    // as the importance picks require) from the lines prefetched into L2
+    if (imp_row) {
+        for (int jj = threadIdx.x; jj < kBlocksPerChunk; jj += kThreads) {
             const int j = blockIdx.x * kBlocksPerChunk + jj;
-            if (j >= nb) break;   // warp-uniform
+            if (j >= nb) break;
             const int p0 = j * BS, p_end = min(p0 + BS, L);
             float sacc = 0.f;
-            for (int base = p0; base < p_end; base += 32) {
-                const float v = base + lane < p_end ? imp[base + lane] : 0.f;
-                const int cnt = min(32, p_end - base);
-                for (int t = 0; t < cnt; ++t) sacc = __fadd_rn(sacc, __shfl_sync(0xffffffffu, v, t));
+            for (int base = p0; base < p_end; base += 16) {
+                float v[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v[t] = base + t < p_end ? imp_row[base + t] : 0.f;
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    if (base + t < p_end) sacc = __fadd_rn(sacc, v[t]);
             }
-            if (lane == 0) {
-                if (MODE != kGlobal) dst_ikeys[j] = float_key(sacc);
-                else a.isum[static_cast<size_t>(u) * a.MKBPR + j] = sacc;
-            }
+            if (MODE != kGlobal) dst_ikeys[j] = float_key(sacc);
+            else a.isum[static_cast<size_t>(u) * a.MKBPR + j] = sacc;
         }
     }
 #pragma unroll
@@ -306,7 +334,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         if (cl == 0 && j < nb) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                if (MODE != kGlobal) dst_pkeys[h * a.MKBPR + j] = float_key(best[h]);
+                if (MODE != kGlobal) dst_pkeys[h * kstr + j] = float_key(best[h]);
                 else a.probe[(static_cast<size_t>(b) * a.H + n * G + h) * a.MKBPR + j] = best[h];
             }
         }
@@ -329,7 +357,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         __threadfence();
         for (int e = threadIdx.x; e < G * nb; e += kThreads) {
             const int h = e / nb, j = e % nb;
-            pkeys[h * a.MKBPR + j] =
+            pkeys[h * kstr + j] =
                 float_key(ldcg_f32(a.probe + (static_cast<size_t>(b) * a.H + n * G + h) * a.MKBPR + j));
         }
         if (a.importance)
@@ -341,12 +369,13 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
 
     // ---- importance pre-selection (same for every head of the request)
     const int n_imp = a.importance ? min((a.k + 1) / 2, nb) : 0;
-    const bool small = nb <= kWarpSmallMax && G <= kThreads / 32;
+    const bool small = nb <= kWarpSmallMax && G * nb <= kThreads * kRankMaxPerThread &&
+                       G <= kThreads / 32;
     for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = kCand;
     __syncthreads();
     if (n_imp > 0) {
         if (small) {
-            if (warp == 0) warp_topk_small(ikeys, imp_flags, nb, n_imp);
+            block_rank_topk<kThreads>(ikeys, 0, imp_flags, 0, nb, 1, n_imp);
             __syncthreads();
         } else {
             topk_fast<kThreads>(ikeys, imp_flags, nb, n_imp, s_fast, s_topk);
@@ -356,17 +385,24 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
         imp_flags[j] = (imp_flags[j] & kPick) ? kFixed : 0;
     const int want = min(a.k - n_imp, nb - n_imp);
     if (small) {
-        // one warp per query head, no block barrier: probe fill, recency,
-        // ordered output
+        // every query head at once: the importance picks leave the candidates
+        // (their keys zeroed), counting top-k over all heads, then one warp
+        // per head for recency and the ordered output
+        __syncthreads();
+        for (int e = threadIdx.x; e < G * nb; e += kThreads) {
+            const int h = e / nb, j = e - h * nb;
+            const bool fixed = imp_flags[j] != 0;
+            flags[static_cast<size_t>(h) * a.MKBPR + j] = fixed ? kFixed : kCand;
+            if (fixed) pkeys[static_cast<size_t>(h) * kstr + j] = 0u;
+        }
+        __syncthreads();
+        block_rank_topk<kThreads>(pkeys, kstr, flags, a.MKBPR, nb, G, want);
         __syncthreads();
         if (warp < G) {
             const int h = warp;
             const size_t row = static_cast<size_t>(b) * a.H + n * G + h;
-            const uint32_t* keys = pkeys + static_cast<size_t>(h) * a.MKBPR;
+            const uint32_t* keys = pkeys + static_cast<size_t>(h) * kstr;
             uint8_t* fl = flags + static_cast<size_t>(h) * a.MKBPR;
-            for (int j = lane; j < nb; j += 32) fl[j] = imp_flags[j] ? kFixed : kCand;
-            __syncwarp();
-            warp_topk_small(keys, fl, nb, want);
             if (want > 0 && !(fl[nb - 1] & (kFixed | kPick))) {
                 // the last block replaces the probe pick with the lowest probe
                 // score (ties: the larger index); importance picks stay
@@ -397,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) probe_select_kernel(ProbeArgs a) {
     // ---- per query head: probe fill, recency insurance, ordered output
     for (int h = 0; h < G; ++h) {
         const size_t row = static_cast<size_t>(b) * a.H + n * G + h;
-        const uint32_t* keys = pkeys + static_cast<size_t>(h) * a.MKBPR;
+        const uint32_t* keys = pkeys + static_cast<size_t>(h) * kstr;
         topk_fast_clear<kThreads>(s_fast, nb);
         for (int j = threadIdx.x; j < nb; j += kThreads) flags[j] = imp_flags[j] ? kFixed : kCand;
         __syncthreads();
@@ -457,7 +493,8 @@ qs_status launch_mode(const ProbeArgs& a, int chunks, size_t smem, cudaStream_t 
 
 template <Dt KT, int D, int G>
 qs_status launch(const ProbeArgs& a, cudaStream_t s) {
-    const size_t smem = align_up(static_cast<size_t>(a.MKBPR) * (4 * G + 4 + G + 1), 16);
+    const size_t kstr = (static_cast<size_t>(a.MKBPR) + 3) & ~static_cast<size_t>(3);
+    const size_t smem = align_up(kstr * (4 * G + 4) + static_cast<size_t>(a.MKBPR) * (G + 1), 16);
     if (smem > 160 * 1024) return QS_EUNSUPPORTED;
     constexpr int kBlocksPerChunk = blocks_per_chunk<KT, D>();
     const int chunks = max(1, (a.MKBPR + kBlocksPerChunk - 1) / kBlocksPerChunk);

@@ -59,12 +59,16 @@ struct SelectArgs {
     int32_t* dev_status;
 };
 
-// Scores rows [j_begin, j_end) of unit (b, n) (steps 1, 2.1, 2.2).  Keys go to
-// keys_s (shared, indexed by row) when given; scores to scores_u (global,
-// indexed by row) when given.
+// Scores every row of unit (b, n), whose rows fit one chunk (steps 1, 2.1,
+// 2.2).  Keys go to keys_s (shared, indexed by row); scores to scores_u
+// (global, indexed by row) when given.  The request's length, the table
+// entries of every row the unit may have and the query slices are requested
+// together, in one round trip, before the length is used; returns false
+// (uniformly) for a length out of range, else the block count in *nb_out and
+// the length in *L_out.
 template <Dt MT, int D>
-QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j_end,
-                           uint32_t* keys_s, float* scores_u) {
+QS_DEVINL bool score_unit(const SelectArgs& a, int b, int n, uint32_t* keys_s, float* scores_u,
+                          int* nb_out, int* L_out) {
     constexpr int kElemBytes = DtInfo<MT>::bytes;
     constexpr int kLanesPerRow = D * kElemBytes / 16;   // 8, 16 or 32
     constexpr int kRowsPerWarp = 32 / kLanesPerRow;
@@ -77,14 +81,13 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
     const int BS = a.BS;
     const size_t head_off = static_cast<size_t>(n) * D * kElemBytes + static_cast<size_t>(cl) * 16;
     const size_t row_stride = static_cast<size_t>(a.N) * D * kElemBytes;
-    // Table entries and the G heads' query slices are all requested before
-    // either is used (in-order issue would otherwise serialise the round
-    // trips); the metadata rows follow once the table entries are back.
+    const int maxnb = a.MMBPR * BS;
+    const int L = ldg_now_s32(a.seq_lens + b);
     int mrow[kUnroll];
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
-        const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
-        mrow[r] = j < j_end ? a.mbt[static_cast<size_t>(b) * a.MMBPR + QS_META_BLOCK(a, j)] : -1;
+        const int j = (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
+        mrow[r] = j < maxnb ? ldg_now_s32(a.mbt + static_cast<size_t>(b) * a.MMBPR + QS_META_BLOCK(a, j)) : -1;
     }
     constexpr int kQBytes = kEl * 4;                 // fp32 query slice; 16-bit uses half
     constexpr int kQVec = (kQBytes + 15) / 16;       // 16-byte loads per head slice
@@ -99,13 +102,17 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
             qraw[g][v] = make_uint4(0, 0, 0, 0);
             if (g < G && v * 16 < kEl * q_es) {
                 const uint8_t* p = qbase + static_cast<size_t>(g) * D * q_es + v * 16;
-                if (kEl * q_es >= 16) qraw[g][v] = *reinterpret_cast<const uint4*>(p);
+                if (kEl * q_es >= 16) qraw[g][v] = ldg_now_v4(p);
                 else {
-                    const uint2 h = *reinterpret_cast<const uint2*>(p);
+                    const uint2 h = ldg_now_v2(p);
                     qraw[g][v] = make_uint4(h.x, h.y, 0, 0);
                 }
             }
         }
+    if (L < 0 || (L + BS - 1) / BS > maxnb) return false;
+    const int nb = (L + BS - 1) / BS;
+    *nb_out = nb;
+    *L_out = L;
     // group-mean query of this lane's slice
     float qreg[kEl];
     {
@@ -138,9 +145,9 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
     bool live[kUnroll];
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
-        const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
+        const int j = (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
         const int m = mrow[r];
-        live[r] = j < j_end;
+        live[r] = j < nb;
         vmx[r] = vmn[r] = make_uint4(0, 0, 0, 0);
         if (live[r]) {
             if (m < 0 || m >= a.num_meta) {
@@ -155,23 +162,26 @@ QS_DEVINL void score_chunk(const SelectArgs& a, int b, int n, int j_begin, int j
     }
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
-        const int j = j_begin + (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
+        const int j = (r * (kThreads / 32) + warp) * kRowsPerWarp + sub;
         const float s = row_score_reduce<kLanesPerRow>(rc.dot(vmx[r], vmn[r]));
-        if (cl == 0 && j < j_end) {
+        if (cl == 0 && j < nb) {
             const float v = live[r] ? s : __int_as_float(0xff800000);
-            if (keys_s) keys_s[j] = float_key(v);
+            keys_s[j] = float_key(v);
             if (scores_u) scores_u[j] = v;
         }
     }
+    return true;
 }
 
 // Forced set, top-k and emission of one unit whose nb keys are in keys_s
 // (step 2.3 + window).  All threads; ends with a barrier.
-// kWarpPath: units of up to kWarpSmallMax blocks select with the one-warp
-// max-extraction top-k (measured faster in the one-CTA-per-unit selector; in
-// the top-k kernel after the scan the histogram levels alone measured faster).
-template <bool kWarpPath>
-QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, const uint32_t* keys_s,
+// kRankPath: units of up to kRankMaxPerThread keys per thread select with the
+// counting top-k over all threads (the forced blocks' keys are zeroed so that
+// they leave the candidates); larger units, and the top-k kernel after the
+// scan, use the histogram levels.  keys_s holds round_up(nb, 4) readable
+// words.
+template <bool kRankPath>
+QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, uint32_t* keys_s,
                            uint8_t* flags, int32_t* sel_out, TopkFastScratch& s_fast,
                            TopkScratch<kThreads>& s_topk) {
     const int w0 = forced_window_start(L, a.BS, nb, a.t);   // nb: no window
@@ -182,18 +192,19 @@ QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, const uint32_t* k
         __syncthreads();
         return;
     }
-    const bool small = kWarpPath && nb <= kWarpSmallMax;
+    const bool small = kRankPath && nb <= kThreads * kRankMaxPerThread;
     if (!small) topk_fast_clear<kThreads>(s_fast, nb);
-    for (int j = threadIdx.x; j < nb; j += kThreads)
-        flags[j] = (a.t >= 0 && (j == 0 || j >= w0)) ? kFixed : kCand;
+    for (int j = threadIdx.x; j < nb; j += kThreads) {
+        const bool forced = a.t >= 0 && (j == 0 || j >= w0);
+        flags[j] = forced ? kFixed : kCand;
+        if (small && forced) keys_s[j] = 0u;
+    }
     __syncthreads();
     const int want = min(a.k - n_forced, nb - n_forced);
     if (small) {
-        // one warp: max-extraction rounds, then the ordered output
-        if (threadIdx.x < 32) {
-            warp_topk_small(keys_s, flags, nb, want);
-            warp_emit_flags(flags, kFixed | kPick, nb, a.k, sel_out);
-        }
+        block_rank_topk<kThreads>(keys_s, 0, flags, 0, nb, 1, want);
+        __syncthreads();
+        if (threadIdx.x < 32) warp_emit_flags(flags, kFixed | kPick, nb, a.k, sel_out);
     } else {
         topk_fast<kThreads>(keys_s, flags, nb, want, s_fast, s_topk);
         block_emit_flags<kThreads>(flags, kFixed | kPick, nb, a.k, sel_out, s_topk);
@@ -211,18 +222,16 @@ __global__ void __launch_bounds__(kThreads, 2) quest_select_unit_kernel(SelectAr
     const int u = blockIdx.x;
     const int b = u / a.N, n = u % a.N;
     const int maxnb = a.MMBPR * a.BS;
-    const int L = a.seq_lens[b];
     int32_t* sel_out = a.selected + static_cast<size_t>(u) * a.k;
-    if (L < 0 || (L + a.BS - 1) / a.BS > maxnb) {
+    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
+    uint8_t* flags = dyn + ((static_cast<size_t>(maxnb) + 3) & ~static_cast<size_t>(3)) * 4;
+    int nb = 0, L = 0;
+    if (!score_unit<MT, D>(a, b, n, keys, a.scores_out ? a.scores + static_cast<size_t>(u) * maxnb : nullptr,
+                           &nb, &L)) {
         if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_ESEQ_LEN);
         for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;
         return;
     }
-    const int nb = (L + a.BS - 1) / a.BS;
-    uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
-    uint8_t* flags = dyn + static_cast<size_t>(maxnb) * 4;
-    score_chunk<MT, D>(a, b, n, 0, nb, keys,
-                       a.scores_out ? a.scores + static_cast<size_t>(u) * maxnb : nullptr);
     __syncthreads();
     select_unit<true>(a, L, nb, keys, flags, sel_out, s_fast, s_topk);
 }
@@ -473,7 +482,7 @@ template <Dt MT, int D>
 qs_status launch(const SelectArgs& a, cudaStream_t s) {
     const int maxnb = a.MMBPR * a.BS;
     constexpr int kRows = rows_per_chunk<MT, D>();
-    const size_t key_smem = align_up(static_cast<size_t>(maxnb) * 5, 16);
+    const size_t key_smem = align_up(align_up(static_cast<size_t>(maxnb), 4) * 4 + maxnb, 16);
     if (key_smem > 100 * 1024) return QS_EUNSUPPORTED;
     if (maxnb <= kRows) {
         auto kern = quest_select_unit_kernel<MT, D>;

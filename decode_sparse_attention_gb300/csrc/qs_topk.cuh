@@ -386,6 +386,52 @@ QS_DEVINL void warp_topk_small(const uint32_t* keys, uint8_t* flags, int n, int 
     __syncwarp();
 }
 
+// Counting top-k over `sets` independent key arrays at once, all threads of
+// the block: entry i of set s is picked when it is a candidate and fewer than
+// `want` candidates of its set precede it (a larger key, or an equal key at
+// a lower index).  Set s has its keys at mkeys + s * kstride and its flags at
+// flags + s * fstride; mkeys holds 0 for every entry that is not a
+// candidate (candidate keys are never 0), so the rank loop reads no flags.
+// The key arrays are read with 16-byte loads: kstride and the arrays' start
+// are multiples of 4 words, and entries n .. round_up(n, 4) - 1 must be
+// readable (their values are ignored).  The cost grows with sets * n * n:
+// callers keep sets * n within kRankMaxPerThread keys per thread.  Each key
+// is ranked by `parts` threads (a power of two, up to 8) that split
+// the comparisons; no barrier inside (callers order the key writes before and
+// the flag reads after with their own).
+constexpr int kRankMaxPerThread = 4;
+template <int NT>
+QS_DEVINL void block_rank_topk(const uint32_t* mkeys, int kstride, uint8_t* flags, int fstride,
+                               int n, int sets, int want) {
+    const int NT_ = static_cast<int>(blockDim.x);
+    const int pairs = sets * n;
+    int parts = 1;
+    while (parts < 8 && pairs * parts * 2 <= NT_) parts <<= 1;
+    const int nq = (n + 3) >> 2;                      // 16-byte groups of keys
+    for (int base = 0; base < pairs * parts; base += NT_) {
+        const int t = base + static_cast<int>(threadIdx.x);
+        const int e = t / parts, part = t - e * parts;  // parts consecutive lanes per key
+        const int s = e / max(n, 1), i = e - s * n;
+        const bool live = e < pairs;
+        const uint32_t* ks = mkeys + static_cast<size_t>(live ? s : 0) * kstride;
+        const uint32_t ki = live ? ks[i] : 0u;
+        int rank = 0;
+        if (live && ki != 0u) {
+            for (int g = part; g < nq; g += parts) {
+                const uint4 k4 = *reinterpret_cast<const uint4*>(ks + 4 * g);
+                const int j = 4 * g;
+                rank += (k4.x > ki) | ((k4.x == ki) & (j < i));
+                rank += (j + 1 < n) & ((k4.y > ki) | ((k4.y == ki) & (j + 1 < i)));
+                rank += (j + 2 < n) & ((k4.z > ki) | ((k4.z == ki) & (j + 2 < i)));
+                rank += (j + 3 < n) & ((k4.w > ki) | ((k4.w == ki) & (j + 3 < i)));
+            }
+        }
+        for (int o = 1; o < parts; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (live && part == 0 && ki != 0u && rank < want)
+            flags[static_cast<size_t>(s) * fstride + i] |= kPick;
+    }
+}
+
 // One warp writes the indices j with (flags[j] & bits) in ascending order
 // into out[0..k), -1 padded; returns their number (in every lane).
 QS_DEVINL int warp_emit_flags(const uint8_t* flags, uint8_t bits, int n, int k, int32_t* out) {
