@@ -48,6 +48,8 @@ struct ProbeArgs {
     float* isum;           // [B*N, MKBPR] block importance sums (global mode)
     uint32_t* counters;    // [B*N]
     int32_t* dev_status;
+    uint32_t imp_smem_off;   // byte offset of the staged importance values in dynamic smem
+    int imp_staged;          // the chunk's importance values fit the staging area
 };
 
 // Launches the selector for one KV dtype and head size; G = H/N in {1,2,4,8}.
@@ -149,13 +151,19 @@ __global__ void __launch_bounds__(kThreads, 1) probe_select_kernel(ProbeArgs a) 
         const int i = threadIdx.x + r * kThreads;
         qbits[r] = i < G * D ? ldg_now_q_bits(a.q, a.q_dt, (static_cast<size_t>(b) * a.H + n * G) * D + i) : 0u;
     }
+    // the chunk's importance values go to shared memory (4-byte cp.async)
     const float* imp_row = a.importance ? a.importance + static_cast<size_t>(b) * a.imp_stride : nullptr;
-    if (imp_row) {
-        const long long t0 = static_cast<long long>(blockIdx.x) * kBlocksPerChunk * BS;
-        const long long t1 = min(static_cast<long long>(a.imp_stride), t0 + static_cast<long long>(kBlocksPerChunk) * BS);
-        for (long long t = t0 + static_cast<long long>(threadIdx.x) * 32; t < t1; t += kThreads * 32)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(imp_row + t));
+    const long long imp_t0 = static_cast<long long>(blockIdx.x) * kBlocksPerChunk * BS;
+    float* s_imp = reinterpret_cast<float*>(dyn + a.imp_smem_off);
+    if (imp_row && a.imp_staged) {
+        const long long t1 = min(static_cast<long long>(a.imp_stride),
+                                 imp_t0 + static_cast<long long>(kBlocksPerChunk) * BS);
+        for (long long t = imp_t0 + threadIdx.x; t < t1; t += kThreads)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(s_imp + (t - imp_t0))),
+                         "l"(imp_row + t)
+                         : "memory");
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     const bool bad_len = L < 0 || L > a.MKBPR * BS ||
                          (a.importance != nullptr && L > a.imp_stride);
     if (bad_len) {   // uniform over the unit's CTAs
@@ -263,21 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1) probe_select_kernel(ProbeArgs a) 
     }
     // importance of this chunk's blocks while the probe rows are in flight:
     // one thread per block, the sum taken in token order (fp32, sequential,
-    // as the importance picks require) from the lines prefetched into L2
+    // as the importance picks require) from the values staged in shared memory
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
     if (imp_row) {
         for (int jj = threadIdx.x; jj < kBlocksPerChunk; jj += kThreads) {
             const int j = blockIdx.x * kBlocksPerChunk + jj;
             if (j >= nb) break;
             const int p0 = j * BS, p_end = min(p0 + BS, L);
+            const float* src = a.imp_staged ? s_imp + (p0 - imp_t0) : imp_row + p0;
             float sacc = 0.f;
-            for (int base = p0; base < p_end; base += 16) {
-                float v[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] = base + t < p_end ? imp_row[base + t] : 0.f;
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (base + t < p_end) sacc = __fadd_rn(sacc, v[t]);
-            }
+#pragma unroll 8
+            for (int t = 0; t < p_end - p0; ++t) sacc = __fadd_rn(sacc, src[t]);
             if (MODE != kGlobal) dst_ikeys[j] = float_key(sacc);
             else a.isum[static_cast<size_t>(u) * a.MKBPR + j] = sacc;
         }
@@ -372,6 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1) probe_select_kernel(ProbeArgs a) 
     const bool small = nb <= kWarpSmallMax && G * nb <= kThreads * kRankMaxPerThread &&
                        G <= kThreads / 32;
     for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = kCand;
+    if (small) {   // the counting top-k reads whole groups of 4 keys: zero padding
+        const int pad = ((nb + 3) & ~3) - nb;
+        for (int e = threadIdx.x; e < (G + 1) * pad; e += kThreads)
+            (e < G * pad ? pkeys + static_cast<size_t>(e / pad) * kstr : ikeys)[nb + e % pad] = 0u;
+    }
     __syncthreads();
     if (n_imp > 0) {
         if (small) {
@@ -493,14 +503,22 @@ qs_status launch_mode(const ProbeArgs& a, int chunks, size_t smem, cudaStream_t 
 
 template <Dt KT, int D, int G>
 qs_status launch(const ProbeArgs& a, cudaStream_t s) {
-    const size_t kstr = (static_cast<size_t>(a.MKBPR) + 3) & ~static_cast<size_t>(3);
-    const size_t smem = align_up(kstr * (4 * G + 4) + static_cast<size_t>(a.MKBPR) * (G + 1), 16);
-    if (smem > 160 * 1024) return QS_EUNSUPPORTED;
     constexpr int kBlocksPerChunk = blocks_per_chunk<KT, D>();
+    const size_t kstr = (static_cast<size_t>(a.MKBPR) + 3) & ~static_cast<size_t>(3);
+    const size_t keys_smem = align_up(kstr * (4 * G + 4) + static_cast<size_t>(a.MKBPR) * (G + 1), 16);
+    // the chunk's importance values are staged in shared memory up to 64 KB
+    // (block sizes beyond that read them from global memory)
+    const size_t imp_bytes = static_cast<size_t>(kBlocksPerChunk) * a.BS * 4;
+    const bool staged = a.importance != nullptr && imp_bytes <= 64 * 1024;
+    const size_t smem = keys_smem + (staged ? imp_bytes : 0);
+    if (smem > 160 * 1024) return QS_EUNSUPPORTED;
+    ProbeArgs a2 = a;
+    a2.imp_smem_off = static_cast<uint32_t>(keys_smem);
+    a2.imp_staged = staged ? 1 : 0;
     const int chunks = max(1, (a.MKBPR + kBlocksPerChunk - 1) / kBlocksPerChunk);
-    if (chunks == 1) return launch_mode<KT, D, G, kSingle>(a, chunks, smem, s);
-    if (chunks <= 8) return launch_mode<KT, D, G, kCluster>(a, chunks, smem, s);
-    return launch_mode<KT, D, G, kGlobal>(a, chunks, smem, s);
+    if (chunks == 1) return launch_mode<KT, D, G, kSingle>(a2, chunks, smem, s);
+    if (chunks <= 8) return launch_mode<KT, D, G, kCluster>(a2, chunks, smem, s);
+    return launch_mode<KT, D, G, kGlobal>(a2, chunks, smem, s);
 }
 
 }  // namespace

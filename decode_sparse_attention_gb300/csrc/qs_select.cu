@@ -176,10 +176,10 @@ QS_DEVINL bool score_unit(const SelectArgs& a, int b, int n, uint32_t* keys_s, f
 // Forced set, top-k and emission of one unit whose nb keys are in keys_s
 // (step 2.3 + window).  All threads; ends with a barrier.
 // kRankPath: units of up to kRankMaxPerThread keys per thread select with the
-// counting top-k over all threads (the forced blocks' keys are zeroed so that
-// they leave the candidates); larger units, and the top-k kernel after the
-// scan, use the histogram levels.  keys_s holds round_up(nb, 4) readable
-// words.
+// counting top-k over all threads (the forced blocks' keys, and the padding
+// up to a multiple of 4 entries, are zeroed so that they leave the
+// candidates); larger units, and the top-k kernel after the scan, use the
+// histogram levels.  keys_s holds round_up(nb, 4) writable words.
 template <bool kRankPath>
 QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, uint32_t* keys_s,
                            uint8_t* flags, int32_t* sel_out, TopkFastScratch& s_fast,
@@ -199,6 +199,7 @@ QS_DEVINL void select_unit(const SelectArgs& a, int L, int nb, uint32_t* keys_s,
         flags[j] = forced ? kFixed : kCand;
         if (small && forced) keys_s[j] = 0u;
     }
+    if (small && static_cast<int>(threadIdx.x) < ((nb + 3) & ~3) - nb) keys_s[nb + threadIdx.x] = 0u;
     __syncthreads();
     const int want = min(a.k - n_forced, nb - n_forced);
     if (small) {
@@ -451,31 +452,41 @@ __global__ void __launch_bounds__(kScanThreads, 1) quest_scan_kernel(SelectArgs 
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// One CTA per unit: the unit's scores (written by the scan) -> forced set,
-// top-k, emission.  Launched as a programmatic dependent of the scan.
+// The units' scores (written by the scan) -> forced set, top-k, emission.
+// Launched as a programmatic dependent of the scan, so its CTAs start while
+// scan CTAs still hold the SMs: left to itself the block scheduler then packs
+// several of them onto the first SMs that free up (measured on GB300: the 64
+// CTAs of the long-context batch on 16 SMs, each running at a quarter of the
+// SM).  So when the units fit on the SMs, each gets a CTA held alone on its
+// SM by a padded shared-memory request; with more units than SMs (where
+// packing costs less than running units one after another: ragged batch,
+// 512 units, 47 vs 58 us) one CTA per unit, unpadded.  Each CTA loops over
+// units all the same.
+constexpr size_t kTopkOnePerSmSmem = 120 * 1024;
 __global__ void __launch_bounds__(kThreads) quest_unit_topk_kernel(SelectArgs a) {
     extern __shared__ __align__(16) uint8_t dyn[];   // keys [maxnb] u32, flags [maxnb] u8
     __shared__ TopkFastScratch s_fast;
     __shared__ TopkScratch<kThreads> s_topk;
     pdl_launch_dependents();
-    const int u = blockIdx.x;
-    const int b = u / a.N;
     const int maxnb = a.MMBPR * a.BS;
-    const int L = a.seq_lens[b];
-    int32_t* sel_out = a.selected + static_cast<size_t>(u) * a.k;
-    pdl_wait();   // the scores are written by the scan
-    if (L < 0 || (L + a.BS - 1) / a.BS > maxnb) {
-        if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_ESEQ_LEN);
-        for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;
-        return;
-    }
-    const int nb = (L + a.BS - 1) / a.BS;
     uint32_t* keys = reinterpret_cast<uint32_t*>(dyn);
     uint8_t* flags = dyn + static_cast<size_t>(maxnb) * 4;
-    const float* scores_u = a.scores + static_cast<size_t>(u) * maxnb;
-    for (int j = threadIdx.x; j < nb; j += kThreads) keys[j] = float_key(ldcg_f32(scores_u + j));
-    __syncthreads();
-    select_unit<false>(a, L, nb, keys, flags, sel_out, s_fast, s_topk);
+    pdl_wait();   // the scores are written by the scan
+    for (int u = blockIdx.x; u < a.B * a.N; u += gridDim.x) {
+        const int b = u / a.N;
+        const int L = a.seq_lens[b];
+        int32_t* sel_out = a.selected + static_cast<size_t>(u) * a.k;
+        if (L < 0 || (L + a.BS - 1) / a.BS > maxnb) {   // uniform over the CTA
+            if (threadIdx.x == 0) set_status(a.dev_status, QS_DEV_ESEQ_LEN);
+            for (int i = threadIdx.x; i < a.k; i += kThreads) sel_out[i] = -1;
+            continue;
+        }
+        const int nb = (L + a.BS - 1) / a.BS;
+        const float* scores_u = a.scores + static_cast<size_t>(u) * maxnb;
+        for (int j = threadIdx.x; j < nb; j += kThreads) keys[j] = float_key(ldcg_f32(scores_u + j));
+        __syncthreads();
+        select_unit<false>(a, L, nb, keys, flags, sel_out, s_fast, s_topk);   // ends with a barrier
+    }
 }
 
 template <Dt MT, int D>
@@ -516,13 +527,16 @@ qs_status launch(const SelectArgs& a, cudaStream_t s) {
     const int grid = static_cast<int>(std::min<long long>(num_sms(), std::max<long long>(chunks, 1)));
     scan<<<grid, kScanThreads, smem, s>>>(a, l);
     QS_CHECK_LAUNCH();
-    // top-k per unit, a programmatic dependent of the scan
+    // top-k per unit, a programmatic dependent of the scan: one CTA per unit,
+    // alone on its SM when the units fit (see quest_unit_topk_kernel)
     auto topk = quest_unit_topk_kernel;
-    if (!ensure_smem(reinterpret_cast<const void*>(topk), key_smem)) return QS_ECUDA;
+    const bool spread = a.B * a.N <= num_sms();
+    const size_t topk_smem = spread ? std::max(key_smem, kTopkOnePerSmSmem) : key_smem;
+    if (!ensure_smem(reinterpret_cast<const void*>(topk), topk_smem)) return QS_ECUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.B * a.N);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.N));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = key_smem;
+    cfg.dynamicSmemBytes = topk_smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -393,12 +393,15 @@ QS_DEVINL void warp_topk_small(const uint32_t* keys, uint8_t* flags, int n, int 
 // flags + s * fstride; mkeys holds 0 for every entry that is not a
 // candidate (candidate keys are never 0), so the rank loop reads no flags.
 // The key arrays are read with 16-byte loads: kstride and the arrays' start
-// are multiples of 4 words, and entries n .. round_up(n, 4) - 1 must be
-// readable (their values are ignored).  The cost grows with sets * n * n:
-// callers keep sets * n within kRankMaxPerThread keys per thread.  Each key
-// is ranked by `parts` threads (a power of two, up to 8) that split
-// the comparisons; no barrier inside (callers order the key writes before and
-// the flag reads after with their own).
+// are multiples of 4 words, and entries n .. round_up(n, 4) - 1 must hold 0.
+// Every entry of a 16-byte group is compared with one threshold: key_i - 1
+// for groups before i's group (an equal key at a lower index precedes),
+// key_i from i's group on; the entries of i's own group before i that equal
+// key_i are added afterwards.  The cost grows with sets * n * n: callers keep
+// sets * n within kRankMaxPerThread keys per thread.  Each key is ranked by
+// `parts` threads (a power of two, up to 8) that split the comparisons; no
+// barrier inside (callers order the key writes before and the flag reads
+// after with their own).
 constexpr int kRankMaxPerThread = 4;
 template <int NT>
 QS_DEVINL void block_rank_topk(const uint32_t* mkeys, int kstride, uint8_t* flags, int fstride,
@@ -411,19 +414,33 @@ QS_DEVINL void block_rank_topk(const uint32_t* mkeys, int kstride, uint8_t* flag
     for (int base = 0; base < pairs * parts; base += NT_) {
         const int t = base + static_cast<int>(threadIdx.x);
         const int e = t / parts, part = t - e * parts;  // parts consecutive lanes per key
-        const int s = e / max(n, 1), i = e - s * n;
         const bool live = e < pairs;
-        const uint32_t* ks = mkeys + static_cast<size_t>(live ? s : 0) * kstride;
+        const int s = live ? e / n : 0, i = live ? e - s * n : 0;
+        const uint32_t* ks = mkeys + static_cast<size_t>(s) * kstride;
         const uint32_t ki = live ? ks[i] : 0u;
         int rank = 0;
-        if (live && ki != 0u) {
-            for (int g = part; g < nq; g += parts) {
-                const uint4 k4 = *reinterpret_cast<const uint4*>(ks + 4 * g);
-                const int j = 4 * g;
-                rank += (k4.x > ki) | ((k4.x == ki) & (j < i));
-                rank += (j + 1 < n) & ((k4.y > ki) | ((k4.y == ki) & (j + 1 < i)));
-                rank += (j + 2 < n) & ((k4.z > ki) | ((k4.z == ki) & (j + 2 < i)));
-                rank += (j + 3 < n) & ((k4.w > ki) | ((k4.w == ki) & (j + 3 < i)));
+        if (ki != 0u) {
+            const uint32_t lo = ki - 1u;
+            const int gi = i >> 2;
+            int r0 = 0, r1 = 0;
+            int g = part;
+            for (; g + parts < nq; g += 2 * parts) {   // two groups per step, two sums
+                const uint4 a = *reinterpret_cast<const uint4*>(ks + 4 * g);
+                const uint4 b = *reinterpret_cast<const uint4*>(ks + 4 * (g + parts));
+                const uint32_t ta = g < gi ? lo : ki, tb = g + parts < gi ? lo : ki;
+                r0 += (a.x > ta) + (a.y > ta) + (a.z > ta) + (a.w > ta);
+                r1 += (b.x > tb) + (b.y > tb) + (b.z > tb) + (b.w > tb);
+            }
+            if (g < nq) {
+                const uint4 a = *reinterpret_cast<const uint4*>(ks + 4 * g);
+                const uint32_t ta = g < gi ? lo : ki;
+                r0 += (a.x > ta) + (a.y > ta) + (a.z > ta) + (a.w > ta);
+            }
+            rank = r0 + r1;
+            if (gi % parts == part) {   // i's group: equal keys before i precede too
+                const int ri = i & 3;
+                const uint32_t* kg = ks + 4 * gi;
+                rank += (0 < ri && kg[0] == ki) + (1 < ri && kg[1] == ki) + (2 < ri && kg[2] == ki);
             }
         }
         for (int o = 1; o < parts; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
