@@ -210,6 +210,17 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 tensor rate for a kernel timed alone: the measured burst
+    figure (MEASURED_PEAKS.json), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("qs_attention.cu", "qs_attention_kernel.cuh", "qs_common.cuh"):
@@ -309,14 +320,36 @@ def metadata_update(w, x, dev, flush, sink, reps=5):
     return statistics.median(times), nbytes
 
 
+def importance_tile_ops(lens, S_max, H, N):
+    """128 x 128 tensor-core tiles the two passes of the prefill importance
+    producer multiply, for prefill lengths `lens` (the loops of its kernels:
+    rows pass, query tile qt against key tiles 0 .. last position / 128;
+    column pass, key tile kt against query tiles kt*G .. (S*G - 1) / 128)."""
+    G = H // N
+    ntq = (S_max * G + 127) // 128
+    ops = 0
+    for S in lens:
+        if S <= 0:
+            continue
+        for qt in range(ntq):
+            if qt * 128 >= S * G:
+                break
+            last_pos = min(qt * 128 + 127, S * G - 1) // G
+            ops += last_pos // 128 + 1
+        for kt in range((S + 127) // 128):
+            ops += max(0, (S * G + 127) // 128 - kt * G)
+    return ops * N
+
+
 def prefill_importance_timing(dev, clocks, reps=5):
     """The prefill importance producer on the probe_importance shape (B=1,
     S=4096, H=16, N=8, D=128, fp32 cache): median of `reps` calls timed with
-    CUDA events after two warm-up calls.  Its inputs (48 MB) are read from L2
-    after the first tile; the kernels are bound by the FP32 pipes, so the
-    roofline is the FP32 FMA rate: SMs x 128 lanes x 2 flop x max SM clock.
-    Algorithmic flops count one logit (2*D) per causal (query row, key) pair;
-    the kernels form every logit twice (row pass, column pass)."""
+    CUDA events after two warm-up calls.  The passes run on the tensor cores
+    (fp32 operands split into bf16 high and low parts, three MMAs per
+    product), so the roofline is the measured dense bf16 rate; executed
+    flops count every 128 x 128 x D tile product the kernels issue (masked
+    parts of diagonal tiles included), algorithmic flops one logit (2*D) per
+    causal (query row, key) pair."""
     from decode_sparse_attention_gb300 import questsparse as qs
     from decode_sparse_attention_gb300 import synth
     w = synth.WORKLOADS["probe_importance"]
@@ -336,21 +369,24 @@ def prefill_importance_timing(dev, clocks, reps=5):
         torch.cuda.synchronize()
         times.append(1000.0 * e0.elapsed_time(e1))
     us = statistics.median(times)
-    pairs = sum(int(S) * (int(S) + 1) // 2 for S in x["seq_lens"].cpu().tolist())
+    lens = x["seq_lens"].cpu().tolist()
+    pairs = sum(int(S) * (int(S) + 1) // 2 for S in lens)
     alg = 2.0 * w.D * w.H * pairs
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    mhz = clocks.get("sm_max_mhz") or 2070.0
-    peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+    products = 3 if x["k_cache"].dtype == torch.float32 else 1
+    executed = importance_tile_ops(lens, S_max, w.H, w.N) * 2.0 * 128 * 128 * w.D * products
+    peak, peak_kind = tensor_peak()
     return {
-        "kernels": "importance_pass_kernel (rows, columns) + importance_sum_kernel",
+        "kernels": "pack_kernel (queries, keys) + importance_tc_kernel (rows, columns) + "
+                   "importance_sum_kernel",
         "workload": "probe_importance prefill: B=1 S=4096 H=16 N=8 D=128 BLOCK_SIZE=32 fp32",
         "us": round(us, 1),
-        "bound": "alu",
+        "bound": "tensor",
         "algorithmic_tflops": round(alg / (us * 1e-6) / 1e12, 2),
-        "executed_tflops": round(2 * alg / (us * 1e-6) / 1e12, 2),
-        "peak_tflops": round(peak, 1),
-        "peak_kind": "derived: %d SMs x 128 FP32 lanes x 2 flop x %.0f MHz" % (sms, mhz),
-        "frac_executed": round(2 * alg / (us * 1e-6) / 1e12 / peak, 4),
+        "executed_tflops": round(executed / (us * 1e-6) / 1e12, 2),
+        "peak_tflops": peak,
+        "peak_kind": peak_kind,
+        "frac_executed": round(executed / (us * 1e-6) / 1e12 / peak, 4),
+        "products_per_logit": products,
         "status": qs.read_status(dev),
     }
 

@@ -20,7 +20,8 @@ PROBE_VARIANTS = [("F32", 128), ("F32", 64), ("BF16", 128), ("BF16", 64), ("F16"
                   ("F16", 64), ("I8", 128)]
 SOURCES = ([(f, os.path.splitext(f)[0], []) for f in
             ["qs_api.cu", "qs_metadata.cu", "qs_select.cu", "qs_probe.cu", "qs_attention.cu",
-             "qs_importance.cu", "qs_attention_noalloc.cu", "qs_step_fused.cu"]] +
+             "qs_importance.cu", "qs_importance_tc.cu", "qs_attention_noalloc.cu",
+             "qs_step_fused.cu"]] +
            [("qs_probe.cu", "qs_probe_%s_%d" % (t, d), ["-DQS_PROBE_KT=%s" % t, "-DQS_PROBE_D=%d" % d])
             for t, d in PROBE_VARIANTS])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

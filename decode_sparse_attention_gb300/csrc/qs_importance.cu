@@ -18,12 +18,13 @@
 // each logit with the same operations in the same order, so pass 2's
 // probabilities are exactly the ones pass 1 normalised.
 //
-// The inputs are fp32 on the pages' engine; tensor cores would round them to
-// tf32/bf16 first, so the contraction stays on the FP32 pipes.
+// This CUDA-core form serves int8 caches; fp32, bf16 and fp16 caches take the
+// tensor-core form (qs_importance_tc.cu), whose passes feed the same column
+// sums into the same final kernel.
 #include <cmath>
 #include <type_traits>
 
-#include "qs_common.cuh"
+#include "qs_internal.cuh"
 
 namespace qs {
 namespace imp {
@@ -566,13 +567,14 @@ using namespace qs::imp;
 
 struct WsPlan {
     int parts, part_tiles;
-    size_t lse2, part, q8, s_q, bytes;
+    size_t lse2, part, q8, s_q, tc, bytes;
 };
 
 // Pass 2 splits each key tile's query range into up to kMaxParts parts of
 // about 16 streamed tiles, so that the keys near the start of a long prefill
 // (seen by every query) do not leave one CTA working long after the rest.
-WsPlan plan_ws(long long B, long long H, long long N, long long D, long long S_max, bool int8) {
+WsPlan plan_ws(long long B, long long H, long long N, long long D, long long S_max, bool int8,
+               bool f32) {
     WsPlan w{};
     const long long G = H / N;
     const long long tq = kStr / G;
@@ -591,6 +593,12 @@ WsPlan plan_ws(long long B, long long H, long long N, long long D, long long S_m
     if (int8) off = align_up(off + static_cast<size_t>(B * S_max * H * D), 256);
     w.s_q = off;
     if (int8) off = align_up(off + static_cast<size_t>(B * S_max * H) * 4, 256);
+    // tensor-core form: packed operand tiles and its own lse2 rows
+    w.tc = off;
+    if (!int8) {
+        size_t oq, ok, ol;
+        off = align_up(off + importance_tc_workspace(B, H, N, D, S_max, f32, &oq, &ok, &ol), 256);
+    }
     w.bytes = off > 0 ? off : 256;
     return w;
 }
@@ -635,7 +643,7 @@ extern "C" qs_status qs_prefill_importance_workspace_size(int32_t B, int32_t H, 
     if (!bytes) return QS_EINVAL;
     const qs_status rc = check_dims(B, H, N, D, S_max);
     if (rc != QS_OK) return rc;
-    *bytes = plan_ws(B, H, N, D, S_max, kv_dtype == QS_I8).bytes;
+    *bytes = plan_ws(B, H, N, D, S_max, kv_dtype == QS_I8, kv_dtype == QS_F32).bytes;
     return QS_OK;
 }
 
@@ -667,7 +675,7 @@ extern "C" qs_status qs_prefill_importance(const void* q, qs_dtype q_dtype, cons
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
          reinterpret_cast<uintptr_t>(workspace)) % 16 != 0)
         return QS_EINVAL;
-    const WsPlan w = plan_ws(B, H, N, D, S_max, int8);
+    const WsPlan w = plan_ws(B, H, N, D, S_max, int8, kv_dtype == QS_F32);
     if (!workspace || workspace_bytes < w.bytes) return QS_EWORKSPACE;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -713,11 +721,13 @@ extern "C" qs_status qs_prefill_importance(const void* q, qs_dtype q_dtype, cons
                 reinterpret_cast<float*>(ws + w.s_q));
     }
     bool ok;
-    switch (kv_dtype) {
-        case QS_F32: ok = launch_d<Dt::F32, Dt::F32>(D, a, st); break;
-        case QS_BF16: ok = launch_d<Dt::BF16, Dt::BF16>(D, a, st); break;
-        case QS_F16: ok = launch_d<Dt::F16, Dt::F16>(D, a, st); break;
-        default: ok = launch_d<Dt::I8, Dt::I8>(D, a, st); break;
+    if (int8) {
+        ok = launch_d<Dt::I8, Dt::I8>(D, a, st);
+    } else {
+        const Dt dt = kv_dtype == QS_F32 ? Dt::F32 : kv_dtype == QS_BF16 ? Dt::BF16 : Dt::F16;
+        ok = importance_tc_launch(q, dt, k_cache, num_kv_blocks, block_tables, MKBPR, prefill_lens,
+                                  S_max, B, H, N, D, BS, a.scale_log2, a.part, w.parts, lse_opt,
+                                  ws + w.tc, dev_status, st);
     }
     if (!ok) return QS_ECUDA;
     const size_t total = static_cast<size_t>(B) * S_max;

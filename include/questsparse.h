@@ -88,7 +88,7 @@ typedef enum {
     QS_DEV_ESEQ_LEN = 3,      /* seq_len < 0 or > MKBPR*BS (or metadata slots)  */
     QS_DEV_ESELECTED = 4,     /* selected index >= ceil(seq_len/BS)             */
     QS_DEV_EFORCED = 5,       /* more forced window blocks than k               */
-    QS_DEV_ETIMEOUT = 6       /* reserved: no kernel of this version waits      */
+    QS_DEV_ETIMEOUT = 6       /* a bounded wait ran out (prefill importance)    */
 } qs_dev_code;
 
 typedef enum {
@@ -335,14 +335,19 @@ qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
  * block_tables[b][s / BS] of k_cache [num_kv_blocks, BS, N, D] (k_scale
  * [num_kv_blocks, BS, N] fp32 for int8).  lse_opt: NULL or [B, H, S_max] fp32,
  * rows i < S receive lse (natural log).  D in {64, 128}; H/N a power of two
- * <= 64; softmax_scale > 0.  Computed in fp32 on the CUDA cores in two passes (row log-sum-exp,
- * then column mass, each recomputing the logits; summation order is the
- * kernel's).  workspace: qs_prefill_importance_workspace_size bytes, no
- * initial contents needed.  Device errors: a table entry outside
+ * <= 64; softmax_scale > 0.  Computed in two passes (row log-sum-exp, then
+ * column mass, each recomputing the logits; summation order is the kernel's):
+ * fp32, bf16 and fp16 caches on the tensor cores (tcgen05, fp32 accumulation;
+ * fp32 operands enter as bf16 high and low parts, three products per q.k
+ * term, relative error near 2^-17 per term; bf16/fp16 products are exact),
+ * int8 caches on the CUDA cores in fp32.  workspace:
+ * qs_prefill_importance_workspace_size bytes (it holds the packed operand
+ * tiles), no initial contents needed.  Device errors: a table entry outside
  * [0, num_kv_blocks) -> QS_DEV_EBLOCK_TABLE (that request's importance is then
  * unspecified; nothing outside the buffers is read or written); S < 0 or
  * S > min(S_max, MKBPR*BS) -> QS_DEV_ESEQ_LEN, and that request's importance
- * is left zero.
+ * is left zero; a bounded wait of the tensor-core passes that runs out ->
+ * QS_DEV_ETIMEOUT (the call's importance is then unspecified).
  */
 qs_status qs_prefill_importance_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D,
                                                int32_t S_max, qs_dtype kv_dtype,

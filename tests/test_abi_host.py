@@ -64,13 +64,20 @@ def test_workspace_size_without_gpu(built_lib):
 
 
 def test_prefill_importance_workspace_without_gpu(built_lib):
-    """Row log-sum-exps (B*H*S_max fp32) plus per-part column sums; int8
-    caches add the quantised query rows and their scales."""
+    """Row log-sum-exps (B*H*S_max fp32) plus per-part column sums; fp32,
+    bf16 and fp16 caches add the packed bf16/fp16 operand tiles of the
+    tensor-core passes (queries B*S_max*H*D and keys B*S_max*N*D elements,
+    two parts for fp32), int8 caches the quantised query rows and their
+    scales."""
     from decode_sparse_attention_gb300 import questsparse as qs
+    base = 16 * 4096 * 4 + 8 * 4096 * 4
+    packed = 4096 * 16 * 128 * 2 + 4096 * 8 * 128 * 2
     f = qs.prefill_importance_workspace_size(1, 16, 8, 128, 4096, qs.F32)
-    assert f >= 16 * 4096 * 4 + 8 * 4096 * 4
+    assert f >= base + 2 * packed
+    h = qs.prefill_importance_workspace_size(1, 16, 8, 128, 4096, qs.BF16)
+    assert base + packed <= h < f
     i8 = qs.prefill_importance_workspace_size(1, 16, 8, 128, 4096, qs.I8)
-    assert i8 >= f + 4096 * 16 * 128 + 4096 * 16 * 4
+    assert i8 >= base + 4096 * 16 * 128 + 4096 * 16 * 4
     with pytest.raises(qs.QuestSparseError):
         qs.prefill_importance_workspace_size(1, 24, 8, 128, 4096, qs.F32)   # H/N = 3
     with pytest.raises(qs.QuestSparseError):

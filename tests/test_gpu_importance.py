@@ -3,9 +3,14 @@
 Small cases (several row, key and query-part tiles, ragged lengths, empty
 requests) are compared element by element with the oracle in double:
 importance within rtol 1e-4 / atol 1e-6 and the row log-sum-exp within
-1e-5 (relative + absolute).  The bound: each logit is an fp32 dot of D
-products (exact for bf16/fp16/int8 operands) with error ~D * 2^-24 relative
-to sum |q_d k_d|, the base-2 exponential is the SFU approximation (~2 ulp),
+1e-5 (relative + absolute).  The bound: each logit is a dot of D products
+accumulated in fp32.  bf16/fp16/int8 products are exact; fp32 operands reach
+the tensor cores as bf16 high and low parts (x = hi + lo + r, |r| <= 2^-18
+|x|) and each product keeps hi.hi + hi.lo + lo.hi, so a product is off by at
+most ~3 * 2^-18 of |q_d k_d|; with the scale 1/sqrt(D) and operands of
+magnitude <= 1 the logit error is a few 1e-6 (the errors of the D terms have
+random signs), and the accumulation adds ~D * 2^-24 relative to
+sum |q_d k_d|.  The base-2 exponential is the SFU approximation (~2 ulp),
 and a token's importance is an fp32 sum of up to G * S probabilities, so the
 relative error stays near 1e-5; 1e-4 leaves a margin of ten.
 
