@@ -779,7 +779,8 @@ def run_ours(args, w):
         "config": dict(head["config"], parallelism="replicas" if ws_ > 1 else "single GPU"),
     }
     for k_ in ("step_gbs", "step_frac_of_peak", "step_frac_of_8tbs", "algorithmic_bytes",
-               "step_us_p10_p50_p90", "step_us_flushed_single", "roofline", "selector",
+               "step_us_p10_p50_p90", "step_us_graph_per_step", "step_us_flushed_single", "roofline",
+               "selector",
                "metadata_prefill_us", "metadata_prefill_gbs", "metadata_update_us",
                "metadata_update_gbs", "metadata_update", "e2e", "clocks", "gpu_launches",
                "cpu_baseline"):
