@@ -17,14 +17,15 @@
 //    relative error near 2^-17 per product against fp32's 2^-24 (the dropped
 //    lo.lo term and the residual of the split).  bf16 and fp16 inputs need
 //    one MMA each and are exact up to the fp32 accumulation.
-//  * Each pass is one CTA per 128-row resident tile: warp 4 loads the
+//  * Each pass is one CTA per 128-row resident tile: warp 8 loads the
 //    resident tile once and streams the other operand's tiles through two
 //    shared-memory slots (cp.async.bulk, mbarrier transaction counts) and one
 //    of its threads issues the MMAs (M = N = 128, K = 16) into one of two
-//    TMEM accumulators; warps 0-3 read the accumulator rows of their TMEM lane
-//    quarter (tcgen05.ld), apply the causal mask and the softmax arithmetic,
-//    and hand the accumulator back.  Loads, MMAs and the epilogue of
-//    consecutive tiles overlap.
+//    TMEM accumulators; warps 0-7 read the accumulator rows of their TMEM lane
+//    quarter (warp w: quarter w % 4, columns 64 * (w / 4) .. +63; tcgen05.ld),
+//    apply the causal mask and the softmax arithmetic, and hand the
+//    accumulator back; the two halves of a row are combined at the end.
+//    Loads, MMAs and the epilogue of consecutive tiles overlap.
 //  * Rows pass: resident = 128 query rows, streamed = key tiles 0 .. last
 //    position; column pass: resident = 128 keys, streamed = the query tiles
 //    that can see them (split into parts as in the CUDA-core form); the
@@ -42,10 +43,11 @@ namespace qs {
 namespace imptc {
 
 constexpr int kRows = 128;                 // tile rows (MMA M and N)
-constexpr int kEpiWarps = 4;               // warps 0-3: TMEM lane quarters
+constexpr int kEpiWarps = 8;               // warps 0-7: two per TMEM lane quarter
 constexpr int kThreads = (kEpiWarps + 1) * 32;
 constexpr int kTmemCols = 256;             // two 128-column fp32 accumulators
-constexpr uint32_t kSpinMax = 1u << 22;    // bounded mbarrier waits
+constexpr uint32_t kSpinMax = 1u << 20;    // bounded mbarrier waits: tries of
+constexpr uint32_t kSuspendNs = 1000;      // at most ~1 us each (about a second)
 constexpr int kCopyPiece = 16 * 1024;      // bytes per bulk copy
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -201,15 +203,16 @@ QS_DEVINL void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // Waits for the completion of the phase with the given parity; false when
-// the bound ran out.
+// the bound ran out (kSpinMax tries, each suspending the thread for at most
+// kSuspendNs unless the phase completes first).
 QS_DEVINL bool mbar_wait(uint32_t bar, uint32_t parity) {
     for (uint32_t it = 0; it < kSpinMax; ++it) {
         uint32_t ok;
         asm volatile(
-            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
             "selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(ok)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (ok) return true;
     }
@@ -248,17 +251,18 @@ QS_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // Shared-memory layout of a pass: resident tile (nsplit parts), two streamed
-// slots, barriers, TMEM address.
+// slots, barriers, TMEM address, the second column halves' row states.
 template <int D>
 struct Smem {
     static constexpr uint32_t tile = kRows * D * 2;
-    uint32_t res, slot0, bars, tmem_ptr, bytes;
+    uint32_t res, slot0, bars, tmem_ptr, half, bytes;
     QS_DEVINL __host__ Smem(int nsplit) {
         res = 0;
         slot0 = res + nsplit * tile;
         bars = slot0 + 2 * nsplit * tile;
         tmem_ptr = bars + 8 * 8;
-        bytes = tmem_ptr + 16;
+        half = tmem_ptr + 16;
+        bytes = half + 2 * kRows * 4;
     }
 };
 
@@ -398,9 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
             }
         }
     } else {
-        // ---- epilogue: accumulator row r = this thread's TMEM lane
-        const int r = warp * 32 + lane;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        // ---- epilogue: accumulator row r = this thread's TMEM lane, column
+        // half hc of every 128-column tile
+        const int quarter = warp & 3, hc = warp >> 2;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const float qf = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f, colsum = 0.f;
         // row pass: query row pr = rt*128 + r; column pass: key s = rt*128 + r
@@ -419,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
             tc_fence_after();
             const int t = t_lo + j;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kRows; c0 += 32) {
+            for (int c0 = hc * 64; c0 < hc * 64 + 64; c0 += 32) {
                 float v[32];
                 tmem_ld32(lane_base + static_cast<uint32_t>(s * kRows + c0), v);
                 if constexpr (!kCols) {
@@ -471,7 +477,25 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty(s));
         }
-        if constexpr (!kCols) {
+        // combine the two column halves of every row (the second half's
+        // state goes through shared memory)
+        float* half_m = reinterpret_cast<float*>(smem + L.half);
+        float* half_x = half_m + kRows;
+        if (hc == 1) {
+            half_m[r] = m_run;
+            half_x[r] = kCols ? colsum : l_run;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+        if (hc == 1) {
+            // nothing more: the first half writes the row
+        } else if constexpr (!kCols) {
+            const float m1 = half_m[r], l1 = half_x[r];
+            const float M = fmaxf(m_run, m1);
+            if (M != -INFINITY) {
+                l_run = (m_run == -INFINITY ? 0.f : l_run * exp2_approx(m_run - M)) +
+                        (m1 == -INFINITY ? 0.f : l1 * exp2_approx(m1 - M));
+                m_run = M;
+            }
             if (pr_res < S * G && !s_fail) {
                 const float l2 = m_run + log2f(l_run);
                 a.lse2[static_cast<size_t>(bn) * a.ls_stride + pr_res] = l2;
@@ -481,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
                 }
             }
         } else if (pr_res < a.S_max) {
-            a.part[(static_cast<size_t>(bn) * a.parts + part) * a.S_max + pr_res] = colsum;
+            a.part[(static_cast<size_t>(bn) * a.parts + part) * a.S_max + pr_res] = colsum + half_x[r];
         }
     }
     tc_fence_before();
@@ -490,6 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
+}
+
+// Self-check of the bounded wait: one thread waits on an mbarrier that
+// nothing arrives on, runs out and records QS_DEV_ETIMEOUT.
+__global__ void bounded_wait_check_kernel(int32_t* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait(smem_addr(&bar), 0)) set_status(status, QS_DEV_ETIMEOUT);
+    }
 }
 
 }  // namespace imptc
@@ -587,3 +622,10 @@ bool importance_tc_launch(const void* q, Dt dt, const void* k_cache, int32_t num
 }
 
 }  // namespace qs
+
+extern "C" qs_status qs_check_bounded_wait(int32_t* dev_status, qs_stream_t stream) {
+    if (!dev_status) return QS_EINVAL;
+    qs::imptc::bounded_wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        dev_status);
+    return cudaGetLastError() == cudaSuccess ? QS_OK : QS_ECUDA;
+}

@@ -85,7 +85,8 @@ def lib():
                                                 I32, I32, I32, F, P, P, P, SZ, P, P]
             L.qs_sparse_decode_step.argtypes = [ctypes.POINTER(StepParams), P]
             L.qs_step_kernels.argtypes = [ctypes.POINTER(StepParams), P]
-            for f in ("qs_read_status", "qs_workspace_size", "qs_prefill_metadata",
+            L.qs_check_bounded_wait.argtypes = [P, P]
+            for f in ("qs_read_status", "qs_workspace_size", "qs_prefill_metadata", "qs_check_bounded_wait",
                       "qs_block_select_paged", "qs_probe_select", "qs_sparse_decode_attn",
                       "qs_sparse_decode_step", "qs_update_metadata", "qs_step_kernels",
                       "qs_prefill_importance_workspace_size", "qs_prefill_importance"):
@@ -177,6 +178,17 @@ def read_status(device=None, reset=True) -> int:
     _check(lib().qs_read_status(_ptr(st), ctypes.byref(code), 1 if reset else 0,
                                 _stream(device)), "qs_read_status")
     return code.value
+
+
+def check_bounded_wait(device=None) -> int:
+    """Runs the device-side bounded-wait self-check on `device` and returns
+    the device code it left (QS_DEV_ETIMEOUT, 6, when the wait ran out as it
+    should)."""
+    device = torch.device(device or "cuda")
+    read_status(device)   # start from a clear status word
+    st = status_word(device)
+    _check(lib().qs_check_bounded_wait(_ptr(st), _stream(device)), "qs_check_bounded_wait")
+    return read_status(device)
 
 
 def device_error_string(code: int) -> str:

@@ -102,6 +102,15 @@ typedef enum {
 /* Library version (major*10000 + minor*100 + patch). */
 int32_t qs_version(void);
 
+/* Self-check of the device-side bounded wait (no counterpart on the pages):
+ * enqueues one small kernel that waits, with the same bounded mbarrier wait
+ * the tensor-core prefill-importance passes use, on a barrier that nothing
+ * arrives on.  The wait runs out after about a second and the kernel stores
+ * QS_DEV_ETIMEOUT into *dev_status (read it with qs_read_status()); the
+ * context stays usable.  dev_status: device int32.  Errors: NULL ->
+ * QS_EINVAL; a launch failure -> QS_ECUDA. */
+qs_status qs_check_bounded_wait(int32_t* dev_status, qs_stream_t stream);
+
 /* Human-readable text for a qs_status or, for values >= 100, for the device
  * code (value - 100).  Never NULL. */
 const char* qs_status_string(int32_t code);

@@ -20,6 +20,8 @@ exactly on a slice: total mass H*S, the log-sum-exp of the first 512 rows
 (causal rows depend only on the prefix), and importance[s] for the last 128
 positions (the oracle summing only the queries from S-128 on).
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -184,3 +186,22 @@ def test_importance_errors_and_empty():
     with pytest.raises(qs.QuestSparseError):
         qs.prefill_importance(q.to(DEV).to(torch.bfloat16), g["k_cache"], g["block_tables"],
                               torch.tensor(lens, dtype=torch.int32, device=DEV))
+
+
+def test_bounded_wait_runs_out_and_reports_timeout():
+    """Every wait of the tensor-core passes is bounded.  The library's
+    self-check runs that same wait on an mbarrier nothing arrives on: it must
+    return within seconds with QS_DEV_ETIMEOUT (6) in the status word, and
+    the context must stay usable (a producer call afterwards still matches
+    the oracle)."""
+    t0 = time.time()
+    assert qs.check_bounded_wait(DEV) == 6
+    assert time.time() - t0 < 30.0
+    w, lens = CASES["f32_d128_g2_bs32"]
+    x, g, q, S_max = inputs(w, lens, 9, DEV)
+    imp, _ = gpu_run(w, g, q, lens)
+    sync_ok()
+    ref, _ = oracle_run(w, x, q, lens)
+    for b, S in enumerate(lens):
+        np.testing.assert_allclose(imp.cpu().double().numpy()[b, :S], ref[b, :S], rtol=RTOL, atol=ATOL)
+
