@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) probe_select_kernel(ProbeArgs a) 
 
     // ---- importance pre-selection (same for every head of the request)
     const int n_imp = a.importance ? min((a.k + 1) / 2, nb) : 0;
-    const bool small = nb <= kWarpSmallMax && G * nb <= kThreads * kRankMaxPerThread &&
+    const bool small = nb <= kProbeRankMax && G * nb <= kThreads * kRankMaxPerThread &&
                        G <= kThreads / 32;
     for (int j = threadIdx.x; j < nb; j += kThreads) imp_flags[j] = kCand;
     if (small) {   // the counting top-k reads whole groups of 4 keys: zero padding

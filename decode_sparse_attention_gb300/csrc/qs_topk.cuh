@@ -342,49 +342,9 @@ QS_DEVINL void topk_fast(const uint32_t* keys, uint8_t* flags, int n, int want,
     __syncthreads();
 }
 
-// One-warp top-k for small units (n <= kWarpSmallMax entries): each lane
-// keeps its entries j = lane + 32*m in registers; every round takes the best
-// remaining candidate of the warp -- the largest key by a hardware warp
-// max-reduction, the lowest index among equal keys by a min-reduction -- so
-// `want` rounds pick exactly the top `want` (key descending, lower index
-// first).  No block barrier: several warps can select for different units
-// or heads at once.  Keys of candidates are never 0 (float_key of a finite
-// or infinite score), so 0 marks "no candidate left".
-constexpr int kWarpSmallMax = 256;
-QS_DEVINL void warp_topk_small(const uint32_t* keys, uint8_t* flags, int n, int want) {
-    constexpr int M = kWarpSmallMax / 32;
-    const int lane = threadIdx.x & 31;
-    uint32_t kv[M];
-    unsigned live = 0;
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-        const int j = lane + 32 * m;
-        kv[m] = 0;
-        if (j < n && (flags[j] & kCand)) {
-            kv[m] = keys[j];
-            live |= 1u << m;
-        }
-    }
-    for (int it = 0; it < want; ++it) {
-        uint32_t bk = 0;
-        int bm = -1;
-#pragma unroll
-        for (int m = 0; m < M; ++m)
-            if (((live >> m) & 1u) && (bm < 0 || kv[m] > bk)) {   // ascending m: lower index on ties
-                bk = kv[m];
-                bm = m;
-            }
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bm >= 0 ? bk : 0u);
-        if (kmax == 0u) break;   // no candidate left (uniform)
-        const uint32_t mine = (bm >= 0 && bk == kmax) ? static_cast<uint32_t>(lane + 32 * bm) : 0xffffffffu;
-        const uint32_t jstar = __reduce_min_sync(0xffffffffu, mine);
-        if (static_cast<uint32_t>(lane) == (jstar & 31u)) {
-            live &= ~(1u << (jstar >> 5));
-            flags[jstar] |= kPick;
-        }
-    }
-    __syncwarp();
-}
+// Largest unit the probe selector ranks with the counting top-k in one pass
+// over its heads (larger units take the histogram levels, one head at a time).
+constexpr int kProbeRankMax = 256;
 
 // Counting top-k over `sets` independent key arrays at once, all threads of
 // the block: entry i of set s is picked when it is a candidate and fewer than
