@@ -67,3 +67,25 @@ def test_max_over_ranks_gloo_world2():
 
 def test_max_over_ranks_single_process_identity():
     assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_importance_tile_ops_counts_causal_tile_pairs():
+    """The executed-flop count of the prefill importance producer: both of its
+    passes multiply every (128-row query tile, 128-key tile) pair that holds
+    at least one causal (row, key) pair, per KV head (a tile pair does when
+    its first key is at or before the position of its last row).  Checked by
+    enumerating the tile pairs, ragged and tile-unaligned lengths included."""
+    import itertools
+    for lens, H, N in (([4096], 16, 8), ([300, 0, 129, 64], 16, 8), ([1500, 1037], 4, 2),
+                       ([150, 33], 32, 4), ([200, 77], 4, 4)):
+        G = H // N
+        S_max = max(lens) + 37
+        want = 0
+        for S in lens:
+            for qt, kt in itertools.product(range((S * G + 127) // 128), range((S + 127) // 128)):
+                rows = range(128 * qt, min(128 * qt + 128, S * G))
+                keys = range(128 * kt, min(128 * kt + 128, S))
+                if any(s <= r // G for r in (rows[-1],) for s in (keys[0],)):
+                    want += 1
+        assert bench.importance_tile_ops(lens, S_max, H, N) == 2 * N * want
+    assert bench.importance_tile_ops([4096], 4096, 16, 8) == 16896
