@@ -1,8 +1,7 @@
 // Prefill importance producer on the tensor cores (tcgen05, sm_103a): the
 // attention mass each prefill token received, per head, summed over the heads
 // (Kestrel-LLM 10-2, section 1, signal 2; section 2, the decode call site
-// that reads prefill_importance).  Same two passes as the CUDA-core form for
-// int8 caches (qs_importance.cu):
+// that reads prefill_importance), for every cache dtype, in two passes:
 //   rows:    lse2[i,g] = log2 sum_{s<=i} 2^(l2[i,g,s])
 //   columns: mass[s]   = sum_{i>=s, g} 2^(l2[i,g,s] - lse2[i,g])
 // with l2 = softmax_scale * log2(e) * (q . k).
@@ -16,7 +15,12 @@
 //    product is then hi.hi + hi.lo + lo.hi (three MMAs), which leaves a
 //    relative error near 2^-17 per product against fp32's 2^-24 (the dropped
 //    lo.lo term and the residual of the split).  bf16 and fp16 inputs need
-//    one MMA each and are exact up to the fp32 accumulation.
+//    one MMA each and are exact up to the fp32 accumulation.  int8 caches
+//    (with the queries quantised per row as the decode calls do) enter as
+//    bf16, which holds every int8 value exactly; a dot of D <= 128 products
+//    of magnitude <= 127^2 stays below 2^24, so the fp32 accumulation is
+//    exact too, and the epilogue applies the query and key scales (packed
+//    next to the tiles) as the logit = scale * (s_q * s_k) * int_dot.
 //  * Each pass is one CTA per 128-row resident tile: warp 8 loads the
 //    resident tile once and streams the other operand's tiles through two
 //    shared-memory slots (cp.async.bulk, mbarrier transaction counts) and one
@@ -28,7 +32,7 @@
 //    Loads, MMAs and the epilogue of consecutive tiles overlap.
 //  * Rows pass: resident = 128 query rows, streamed = key tiles 0 .. last
 //    position; column pass: resident = 128 keys, streamed = the query tiles
-//    that can see them (split into parts as in the CUDA-core form); the
+//    that can see them (split into parts of the query range); the
 //    epilogue reads the rows' lse2 values, written by the rows pass, from
 //    global memory (uniform loads, L2-resident).
 //  * Every wait is bounded: on running out it records QS_DEV_ETIMEOUT and the
@@ -54,6 +58,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct TcArgs {
     const uint8_t* qpack;     // [B*N, ntq, nsplit] tiles of 128 x D bf16
     const uint8_t* kpack;     // [B*N, ntk, nsplit] tiles
+    const float* qscale;      // int8: [B*N, ntq*128] query-row scales (packed row order)
+    const float* kscale;      // int8: [B*N, ntk*128] key scales
     float* lse2;              // [B*N, ls_stride] base-2 row log-sum-exps, row = i*G + g
     float* part;              // [B*N, parts, S_max] column sums
     float* lse_out;           // optional [B, H, S_max] natural log-sum-exps
@@ -73,6 +79,8 @@ QS_DEVINL bool len_ok(const TcArgs& a, int S) {
 
 struct PackArgs {
     const uint8_t* src;       // queries [B, S_max, H, D] or the paged key cache [P, BS, N, D]
+    const float* scale;       // int8: query scales [B, S_max, H] or key scales [P, BS, N]
+    float* scale_dst;         // int8: the rows' scales in packed order [B*N, ntiles*128]
     const int32_t* bt;        // [B, MKBPR] (keys)
     const int32_t* lens;
     uint8_t* dst;
@@ -107,25 +115,35 @@ __global__ void pack_kernel(const PackArgs a) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = 0.f;
         const uint8_t* src = nullptr;
+        size_t row_idx = 0;                           // the row's scale index (int8)
         if (ok) {
             if constexpr (!kKeys) {
                 if (pr < S * a.G) {
                     const int i = pr / a.G, g = pr - i * a.G;
-                    src = a.src + ((static_cast<size_t>(b) * a.S_max + i) * a.H + n * a.G + g) *
-                                      static_cast<size_t>(D) * DtInfo<T>::bytes;
+                    row_idx = (static_cast<size_t>(b) * a.S_max + i) * a.H + n * a.G + g;
+                    src = a.src + row_idx * static_cast<size_t>(D) * DtInfo<T>::bytes;
                 }
             } else if (pr < S) {
                 const int e = a.bt[static_cast<size_t>(b) * a.MKBPR + pr / a.BS];
                 if (e < 0 || e >= a.P) {
                     if (c == 0) set_status(a.status, QS_DEV_EBLOCK_TABLE);
                 } else {
-                    src = a.src + ((static_cast<size_t>(e) * a.BS + pr % a.BS) * a.N + n) *
-                                      static_cast<size_t>(D) * DtInfo<T>::bytes;
+                    row_idx = (static_cast<size_t>(e) * a.BS + pr % a.BS) * a.N + n;
+                    src = a.src + row_idx * static_cast<size_t>(D) * DtInfo<T>::bytes;
                 }
             }
         }
+        if constexpr (T == Dt::I8) {
+            if (c == 0) a.scale_dst[static_cast<size_t>(tile_lin) * kRows + r] = src ? a.scale[row_idx] : 0.f;
+        }
         if (src) {
-            if constexpr (T == Dt::F32) {
+            if constexpr (T == Dt::I8) {
+                const uint2 u = *reinterpret_cast<const uint2*>(src + c * 8);
+                const uint32_t wv[2] = {u.x, u.y};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    x[e] = static_cast<float>(static_cast<int8_t>((wv[e >> 2] >> (8 * (e & 3))) & 0xffu));
+            } else if constexpr (T == Dt::F32) {
                 const uint4 u0 = *reinterpret_cast<const uint4*>(src + c * 32);
                 const uint4 u1 = *reinterpret_cast<const uint4*>(src + c * 32 + 16);
                 const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -269,7 +287,7 @@ struct Smem {
 // One pass.  kCols = false: rows pass (resident query tile qt, streamed key
 // tiles); kCols = true: column pass (resident key tile, streamed query tiles
 // of this part).
-template <int D, bool kCols>
+template <int D, bool kCols, bool kI8>
 __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs a, uint32_t fmt) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const Smem<D> L(a.nsplit);
@@ -407,11 +425,23 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
         const int quarter = warp & 3, hc = warp >> 2;
         const int r = quarter * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const float qf = a.scale_log2;
+        float qf = a.scale_log2;
         float m_run = -INFINITY, l_run = 0.f, colsum = 0.f;
         // row pass: query row pr = rt*128 + r; column pass: key s = rt*128 + r
         const int pr_res = rt * kRows + r;
         const int i_res = pr_res >> a.g_shift;
+        // int8: the resident row's scale (query: folded into qf; key: kf_res)
+        float kf_res = 1.f;
+        const float* str_scale = nullptr;   // the streamed rows' scales
+        if constexpr (kI8) {
+            if constexpr (!kCols) {
+                qf = __fmul_rn(a.qscale[static_cast<size_t>(bn) * a.ntq * kRows + pr_res], a.scale_log2);
+                str_scale = a.kscale + static_cast<size_t>(bn) * a.ntk * kRows;
+            } else {
+                kf_res = a.kscale[static_cast<size_t>(bn) * a.ntk * kRows + pr_res];
+                str_scale = a.qscale + static_cast<size_t>(bn) * a.ntq * kRows;
+            }
+        }
         for (int j = 0; j < nt; ++j) {
             const int s = j & 1;
             const uint32_t use = static_cast<uint32_t>(j >> 1);
@@ -427,17 +457,31 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
 #pragma unroll 1
             for (int c0 = hc * 64; c0 < hc * 64 + 64; c0 += 32) {
                 float v[32];
+                float sc[32];   // int8: the streamed rows' scales of these columns
+                if constexpr (kI8) {
+                    const float4* s4 = reinterpret_cast<const float4*>(str_scale + static_cast<size_t>(t) * kRows + c0);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 w4 = __ldg(s4 + q4);
+                        sc[4 * q4] = w4.x; sc[4 * q4 + 1] = w4.y; sc[4 * q4 + 2] = w4.z; sc[4 * q4 + 3] = w4.w;
+                    }
+                }
                 tmem_ld32(lane_base + static_cast<uint32_t>(s * kRows + c0), v);
                 if constexpr (!kCols) {
                     // keys t*128 + c0 + jj <= i (and the row exists)
                     const int k0 = t * kRows + c0;
                     const bool row_ok = pr_res < S * G;
+                    if constexpr (kI8) {
+                        // logit (base 2) = (dot * s_q * scale * log2 e) * s_k
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) v[jj] = __fmul_rn(__fmul_rn(v[jj], qf), sc[jj]);
+                    }
                     float cmax = -INFINITY;
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj)
                         if (row_ok && k0 + jj <= i_res) cmax = fmaxf(cmax, v[jj]);
                     if (cmax != -INFINITY) {
-                        const float mt = __fmul_rn(cmax, qf);
+                        const float mt = kI8 ? cmax : __fmul_rn(cmax, qf);
                         if (mt > m_run) {
                             l_run *= exp2_approx(m_run - mt);
                             m_run = mt;
@@ -445,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
                         float add = 0.f;
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) {
-                            const float p = exp2_approx(fmaf(v[jj], qf, -m_run));
+                            const float p = kI8 ? exp2_approx(v[jj] - m_run) : exp2_approx(fmaf(v[jj], qf, -m_run));
                             add += (k0 + jj <= i_res) ? p : 0.f;
                         }
                         l_run += add;
@@ -467,7 +511,11 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) {
                             const int pr = pr0 + jj;
-                            const float p = exp2_approx(fmaf(v[jj], qf, -lse[jj]));
+                            float p;
+                            if constexpr (kI8)
+                                p = exp2_approx(__fmul_rn(__fmul_rn(v[jj], __fmul_rn(sc[jj], qf)), kf_res) - lse[jj]);
+                            else
+                                p = exp2_approx(fmaf(v[jj], qf, -lse[jj]));
                             colsum += (pr >= pr_min && pr < pr_end) ? p : 0.f;
                         }
                     }
@@ -547,8 +595,9 @@ bool launch_tc_dt(const TcArgs& a, const PackArgs& pq, const PackArgs& pk, cudaS
     pack_kernel<T, D, false><<<grid_of(static_cast<long long>(a.B) * a.N * a.ntq * per_tile), 256, 0, st>>>(pq);
     pack_kernel<T, D, true><<<grid_of(static_cast<long long>(a.B) * a.N * a.ntk * per_tile), 256, 0, st>>>(pk);
     const Smem<D> L(a.nsplit);
-    auto k_rows = importance_tc_kernel<D, false>;
-    auto k_cols = importance_tc_kernel<D, true>;
+    constexpr bool kI8 = T == Dt::I8;
+    auto k_rows = importance_tc_kernel<D, false, kI8>;
+    auto k_cols = importance_tc_kernel<D, true, kI8>;
     if (!ensure_smem(reinterpret_cast<const void*>(k_rows), L.bytes) ||
         !ensure_smem(reinterpret_cast<const void*>(k_cols), L.bytes))
         return false;
@@ -562,7 +611,8 @@ bool launch_tc_dt(const TcArgs& a, const PackArgs& pq, const PackArgs& pk, cudaS
 }  // namespace
 
 size_t importance_tc_workspace(long long B, long long H, long long N, long long D, long long S_max,
-                               bool f32, size_t* off_q, size_t* off_k, size_t* off_lse) {
+                               bool f32, bool int8, size_t* off_q, size_t* off_k, size_t* off_lse,
+                               size_t* off_qs, size_t* off_ks) {
     const long long G = H / N;
     const long long ntq = (S_max * G + kRows - 1) / kRows, ntk = (S_max + kRows - 1) / kRows;
     const size_t tile = static_cast<size_t>(kRows) * D * 2 * (f32 ? 2 : 1);
@@ -573,16 +623,21 @@ size_t importance_tc_workspace(long long B, long long H, long long N, long long 
     off = align_up(off + static_cast<size_t>(B * N * ntk) * tile, 256);
     *off_lse = off;
     off = align_up(off + static_cast<size_t>(B * N * ntq) * kRows * 4, 256);
+    // int8: the rows' scales in packed order
+    *off_qs = off;
+    if (int8) off = align_up(off + static_cast<size_t>(B * N * ntq) * kRows * 4, 256);
+    *off_ks = off;
+    if (int8) off = align_up(off + static_cast<size_t>(B * N * ntk) * kRows * 4, 256);
     return off;
 }
 
-bool importance_tc_launch(const void* q, Dt dt, const void* k_cache, int32_t num_kv_blocks,
-                          const int32_t* block_tables, int32_t MKBPR, const int32_t* lens,
-                          int32_t S_max, int32_t B, int32_t H, int32_t N, int32_t D, int32_t BS,
-                          float scale_log2, float* part, int parts, float* lse_out, uint8_t* ws,
-                          int32_t* status, cudaStream_t st) {
-    size_t oq, ok_, ol;
-    importance_tc_workspace(B, H, N, D, S_max, dt == Dt::F32, &oq, &ok_, &ol);
+bool importance_tc_launch(const void* q, const float* q_scale, Dt dt, const void* k_cache,
+                          const float* k_scale, int32_t num_kv_blocks, const int32_t* block_tables,
+                          int32_t MKBPR, const int32_t* lens, int32_t S_max, int32_t B, int32_t H,
+                          int32_t N, int32_t D, int32_t BS, float scale_log2, float* part, int parts,
+                          float* lse_out, uint8_t* ws, int32_t* status, cudaStream_t st) {
+    size_t oq, ok_, ol, oqs, oks;
+    importance_tc_workspace(B, H, N, D, S_max, dt == Dt::F32, dt == Dt::I8, &oq, &ok_, &ol, &oqs, &oks);
     const int G = H / N;
     TcArgs a{};
     a.ntq = static_cast<int>((static_cast<long long>(S_max) * G + kRows - 1) / kRows);
@@ -591,6 +646,8 @@ bool importance_tc_launch(const void* q, Dt dt, const void* k_cache, int32_t num
     a.ls_stride = a.ntq * kRows;
     a.qpack = ws + oq;
     a.kpack = ws + ok_;
+    a.qscale = reinterpret_cast<const float*>(ws + oqs);
+    a.kscale = reinterpret_cast<const float*>(ws + oks);
     a.lse2 = reinterpret_cast<float*>(ws + ol);
     a.part = part;
     a.lse_out = lse_out;
@@ -605,11 +662,15 @@ bool importance_tc_launch(const void* q, Dt dt, const void* k_cache, int32_t num
 
     PackArgs pq{};
     pq.src = static_cast<const uint8_t*>(q);
+    pq.scale = q_scale;
+    pq.scale_dst = reinterpret_cast<float*>(ws + oqs);
     pq.lens = lens; pq.dst = ws + oq; pq.status = status;
     pq.B = B; pq.H = H; pq.N = N; pq.G = G; pq.S_max = S_max; pq.MKBPR = MKBPR; pq.BS = BS;
     pq.P = num_kv_blocks; pq.ntiles = a.ntq; pq.nsplit = a.nsplit;
     PackArgs pk = pq;
     pk.src = static_cast<const uint8_t*>(k_cache);
+    pk.scale = k_scale;
+    pk.scale_dst = reinterpret_cast<float*>(ws + oks);
     pk.bt = block_tables;
     pk.dst = ws + ok_;
     pk.ntiles = a.ntk;
@@ -617,6 +678,7 @@ bool importance_tc_launch(const void* q, Dt dt, const void* k_cache, int32_t num
     switch (dt) {
         case Dt::F32: return D == 64 ? launch_tc_dt<Dt::F32, 64>(a, pq, pk, st) : launch_tc_dt<Dt::F32, 128>(a, pq, pk, st);
         case Dt::BF16: return D == 64 ? launch_tc_dt<Dt::BF16, 64>(a, pq, pk, st) : launch_tc_dt<Dt::BF16, 128>(a, pq, pk, st);
+        case Dt::I8: return D == 64 ? launch_tc_dt<Dt::I8, 64>(a, pq, pk, st) : launch_tc_dt<Dt::I8, 128>(a, pq, pk, st);
         default: return D == 64 ? launch_tc_dt<Dt::F16, 64>(a, pq, pk, st) : launch_tc_dt<Dt::F16, 128>(a, pq, pk, st);
     }
 }

@@ -44,16 +44,19 @@ qs_status sparse_attn_impl(const void* q, qs_dtype q_dtype, const void* k_cache,
 // inputs would make either kernel of the two-kernel step report an error;
 // the caller then runs the two-kernel step.  attn_ws: the attention part of
 // the step's workspace.  launch = false only decides (*taken).
-// Prefill importance on the tensor cores (fp32, bf16, fp16 caches): packs the
+// Prefill importance on the tensor cores (every cache dtype): packs the
 // operands into ws, writes the column sums of every (request, KV head, part)
 // into part and the optional natural log-sum-exps; false on a launch error.
 size_t importance_tc_workspace(long long B, long long H, long long N, long long D, long long S_max,
-                               bool f32, size_t* off_q, size_t* off_k, size_t* off_lse);
-bool importance_tc_launch(const void* q, Dt dt, const void* k_cache, int32_t num_kv_blocks,
-                          const int32_t* block_tables, int32_t MKBPR, const int32_t* lens,
-                          int32_t S_max, int32_t B, int32_t H, int32_t N, int32_t D, int32_t BS,
-                          float scale_log2, float* part, int parts, float* lse_out, uint8_t* ws,
-                          int32_t* status, cudaStream_t st);
+                               bool f32, bool int8, size_t* off_q, size_t* off_k, size_t* off_lse,
+                               size_t* off_qs, size_t* off_ks);
+// int8 (dt = I8): q holds the quantised query rows [B, S_max, H, D] and
+// q_scale their scales [B, S_max, H]; k_scale the cache's [P, BS, N] scales.
+bool importance_tc_launch(const void* q, const float* q_scale, Dt dt, const void* k_cache,
+                          const float* k_scale, int32_t num_kv_blocks, const int32_t* block_tables,
+                          int32_t MKBPR, const int32_t* lens, int32_t S_max, int32_t B, int32_t H,
+                          int32_t N, int32_t D, int32_t BS, float scale_log2, float* part, int parts,
+                          float* lse_out, uint8_t* ws, int32_t* status, cudaStream_t st);
 
 qs_status quest_step_fused(const qs_step_params* p, void* attn_ws, size_t attn_ws_bytes,
                            cudaStream_t stream, bool* taken, bool launch);

@@ -345,11 +345,12 @@ qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
  * [num_kv_blocks, BS, N] fp32 for int8).  lse_opt: NULL or [B, H, S_max] fp32,
  * rows i < S receive lse (natural log).  D in {64, 128}; H/N a power of two
  * <= 64; softmax_scale > 0.  Computed in two passes (row log-sum-exp, then
- * column mass, each recomputing the logits; summation order is the kernel's):
- * fp32, bf16 and fp16 caches on the tensor cores (tcgen05, fp32 accumulation;
- * fp32 operands enter as bf16 high and low parts, three products per q.k
- * term, relative error near 2^-17 per term; bf16/fp16 products are exact),
- * int8 caches on the CUDA cores in fp32.  workspace:
+ * column mass, each recomputing the logits; summation order is the kernel's)
+ * on the tensor cores (tcgen05, fp32 accumulation): fp32 operands enter as
+ * bf16 high and low parts, three products per q.k term, relative error near
+ * 2^-17 per term; bf16/fp16 products are exact; int8 operands enter as bf16
+ * (exact), their dot products are exact, and the scales are applied after
+ * them.  workspace:
  * qs_prefill_importance_workspace_size bytes (it holds the packed operand
  * tiles), no initial contents needed.  Device errors: a table entry outside
  * [0, num_kv_blocks) -> QS_DEV_EBLOCK_TABLE (that request's importance is then
