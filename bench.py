@@ -30,7 +30,10 @@ JSON line keys: metric, value (us per step, lower is better), unit, roofline
 (attention kernel vs the measured HBM copy bandwidth), selector (its own
 bytes and rate), cpu_baseline (the reference oracle on the host, bounded
 sample, with the CPU model and core count), e2e (the same step through the C
-ABI from pinned host buffers, copies included), clocks, gpu_launches, configs.
+ABI from pinned host buffers, copies included), clocks, gpu_launches, configs,
+prefill_importance and prefill_importance_i8 (the tensor-core importance
+producer on the fp32 and int8 probe prefills, against the measured bf16
+tensor rate).
 """
 from __future__ import annotations
 
@@ -341,30 +344,33 @@ def importance_tile_ops(lens, S_max, H, N):
     return ops * N
 
 
-def prefill_importance_timing(dev, clocks, reps=5):
-    """The prefill importance producer on the probe_importance shape (B=1,
-    S=4096, H=16, N=8, D=128, fp32 cache): median of `reps` calls timed with
-    CUDA events after two warm-up calls.  The passes run on the tensor cores
-    (fp32 operands split into bf16 high and low parts, three MMAs per
-    product), so the roofline is the measured dense bf16 rate; executed
-    flops count every 128 x 128 x D tile product the kernels issue (masked
-    parts of diagonal tiles included), algorithmic flops one logit (2*D) per
-    causal (query row, key) pair."""
+def prefill_importance_timing(dev, workload="probe_importance", reps=5):
+    """The prefill importance producer on the prefill of a probe workload
+    (B=1, S=4096, H=16, N=8, D=128; fp32 cache for probe_importance, int8
+    for probe_importance_i8): median of `reps` calls timed with CUDA events
+    after two warm-up calls.  The passes run on the tensor cores (fp32
+    operands split into bf16 high and low parts, three MMAs per product;
+    int8 operands are exact in bf16, one MMA), so the roofline is the
+    measured dense bf16 rate; executed flops count every 128 x 128 x D tile
+    product the kernels issue (masked parts of diagonal tiles included),
+    algorithmic flops one logit (2*D) per causal (query row, key) pair."""
     from decode_sparse_attention_gb300 import questsparse as qs
     from decode_sparse_attention_gb300 import synth
-    w = synth.WORKLOADS["probe_importance"]
+    w = synth.WORKLOADS[workload]
     x = synth.make(w, seed=0, device=dev)
     S_max = x["MKBPR"] * w.BS
     q = synth.prefill_queries(w, S_max, seed=0, device=dev)
+    int8 = x["k_cache"].dtype == torch.int8
     args = (q, x["k_cache"], x["block_tables"], x["seq_lens"])
+    kw = {"k_scale": x["k_scale"]} if int8 else {}
     for _ in range(2):
-        qs.prefill_importance(*args)
+        qs.prefill_importance(*args, **kw)
     torch.cuda.synchronize()
     times = []
     for _ in range(reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        qs.prefill_importance(*args)
+        qs.prefill_importance(*args, **kw)
         e1.record()
         torch.cuda.synchronize()
         times.append(1000.0 * e0.elapsed_time(e1))
@@ -375,10 +381,15 @@ def prefill_importance_timing(dev, clocks, reps=5):
     products = 3 if x["k_cache"].dtype == torch.float32 else 1
     executed = importance_tile_ops(lens, S_max, w.H, w.N) * 2.0 * 128 * 128 * w.D * products
     peak, peak_kind = tensor_peak()
+    cache = {torch.float32: "fp32", torch.int8: "int8", torch.bfloat16: "bf16",
+             torch.float16: "fp16"}[x["k_cache"].dtype]
+    packing = "pack_kernel (queries, keys)"
+    if int8:
+        packing = "quantize_rows_kernel (queries) + " + packing
     return {
-        "kernels": "pack_kernel (queries, keys) + importance_tc_kernel (rows, columns) + "
-                   "importance_sum_kernel",
-        "workload": "probe_importance prefill: B=1 S=4096 H=16 N=8 D=128 BLOCK_SIZE=32 fp32",
+        "kernels": packing + " + importance_tc_kernel (rows, columns) + importance_sum_kernel",
+        "workload": "%s prefill: B=%d S=%d H=%d N=%d D=%d BLOCK_SIZE=%d %s cache, %s queries" % (
+            workload, w.B, S_max, w.H, w.N, w.D, w.BS, cache, str(q.dtype).replace("torch.", "")),
         "us": round(us, 1),
         "bound": "tensor",
         "algorithmic_tflops": round(alg / (us * 1e-6) / 1e12, 2),
@@ -787,7 +798,11 @@ def run_ours(args, w):
         if k_ in head:
             res[k_] = head[k_]
     if rank == 0 and not args.no_importance:
-        res["prefill_importance"] = prefill_importance_timing(dev, head["clocks"])
+        which = [v for v in args.importance.split(",") if v]
+        if "fp32" in which:
+            res["prefill_importance"] = prefill_importance_timing(dev, "probe_importance")
+        if "int8" in which:
+            res["prefill_importance_i8"] = prefill_importance_timing(dev, "probe_importance_i8")
     res["configs"] = subs
     if ws_ > 1:
         import torch.distributed as dist
@@ -933,6 +948,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-importance", action="store_true",
                     help="skip timing the prefill importance producer")
+    ap.add_argument("--importance", default="fp32,int8",
+                    help="comma list of the importance producer timings to run: fp32 "
+                         "(probe_importance prefill), int8 (probe_importance_i8 prefill)")
     ap.add_argument("--max-sets", type=int, default=128,
                     help="most input sets to rotate through; workloads needing more (tiny "
                          "steps) are timed with an L2 flush between steps instead")
