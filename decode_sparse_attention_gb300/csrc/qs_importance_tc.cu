@@ -13,8 +13,9 @@
 //    no swizzle), so that a pass loads a tile with bulk copies.  fp32 inputs
 //    are split into a high part bf16(x) and a low part bf16(x - high); a dot
 //    product is then hi.hi + hi.lo + lo.hi (three MMAs), which leaves a
-//    relative error near 2^-17 per product against fp32's 2^-24 (the dropped
-//    lo.lo term and the residual of the split).  bf16 and fp16 inputs need
+//    relative error of at most 2^-15 per product against fp32's 2^-24 (the
+//    dropped lo.lo term, <= 2^-16, and the split residuals, <= 2^-17 each;
+//    the median is near 2^-19).  bf16 and fp16 inputs need
 //    one MMA each and are exact up to the fp32 accumulation.  int8 caches
 //    (with the queries quantised per row as the decode calls do) enter as
 //    bf16, which holds every int8 value exactly; a dot of D <= 128 products

@@ -347,8 +347,8 @@ qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
  * <= 64; softmax_scale > 0.  Computed in two passes (row log-sum-exp, then
  * column mass, each recomputing the logits; summation order is the kernel's)
  * on the tensor cores (tcgen05, fp32 accumulation): fp32 operands enter as
- * bf16 high and low parts, three products per q.k term, relative error near
- * 2^-17 per term; bf16/fp16 products are exact; int8 operands enter as bf16
+ * bf16 high and low parts, three products per q.k term, relative error at
+ * most 2^-15 per term (median near 2^-19); bf16/fp16 products are exact; int8 operands enter as bf16
  * (exact), their dot products are exact, and the scales are applied after
  * them.  workspace:
  * qs_prefill_importance_workspace_size bytes (it holds the packed operand
