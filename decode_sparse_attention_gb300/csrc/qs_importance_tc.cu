@@ -33,9 +33,10 @@
 //    Loads, MMAs and the epilogue of consecutive tiles overlap.
 //  * Rows pass: resident = 128 query rows, streamed = key tiles 0 .. last
 //    position; column pass: resident = 128 keys, streamed = the query tiles
-//    that can see them (split into parts of the query range); the
-//    epilogue reads the rows' lse2 values, written by the rows pass, from
-//    global memory (uniform loads, L2-resident).
+//    that can see them (split into parts of the query range); the rows'
+//    lse2 values, written by the rows pass (and, for int8, the streamed
+//    rows' scales), reach each epilogue warp's shared buffer one tile ahead
+//    through cp.async.
 //  * Every wait is bounded: on running out it records QS_DEV_ETIMEOUT and the
 //    CTA leaves its work, freeing its TMEM.
 #include <cuda_bf16.h>
@@ -54,6 +55,9 @@ constexpr int kTmemCols = 256;             // two 128-column fp32 accumulators
 constexpr uint32_t kSpinMax = 1u << 20;    // bounded mbarrier waits: tries of
 constexpr uint32_t kSuspendNs = 1000;      // at most ~1 us each (about a second)
 constexpr int kCopyPiece = 16 * 1024;      // bytes per bulk copy
+constexpr int kHalfCols = 64;              // accumulator columns of one epilogue warp
+// per epilogue warp: two tiles x (row values, scales) of its 64 columns
+constexpr uint32_t kStageBytes = 2 * 2 * kHalfCols * 4;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct TcArgs {
@@ -269,19 +273,29 @@ QS_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only) and its groups.
+QS_DEVINL void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+QS_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+QS_DEVINL void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+QS_DEVINL void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Shared-memory layout of a pass: resident tile (nsplit parts), two streamed
-// slots, barriers, TMEM address, the second column halves' row states.
+// slots, barriers, TMEM address, the second column halves' row states, the
+// epilogue warps' staging buffers.
 template <int D>
 struct Smem {
     static constexpr uint32_t tile = kRows * D * 2;
-    uint32_t res, slot0, bars, tmem_ptr, half, bytes;
+    uint32_t res, slot0, bars, tmem_ptr, half, stage, bytes;
     QS_DEVINL __host__ Smem(int nsplit) {
         res = 0;
         slot0 = res + nsplit * tile;
         bars = slot0 + 2 * nsplit * tile;
         tmem_ptr = bars + 8 * 8;
         half = tmem_ptr + 16;
-        bytes = half + 2 * kRows * 4;
+        stage = half + 2 * kRows * 4;
+        bytes = stage + kEpiWarps * kStageBytes;
     }
 };
 
@@ -443,9 +457,29 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
                 str_scale = a.qscale + static_cast<size_t>(bn) * a.ntq * kRows;
             }
         }
+        // The per-column values of a streamed tile (column pass: the query
+        // rows' lse2; int8: the streamed rows' scales) are staged in this
+        // warp's shared buffer one tile ahead with cp.async (lanes 0-15:
+        // lse2, lanes 16-31: scales; 16 bytes each), so the epilogue reads
+        // them from shared memory instead of waiting on L2 every tile.
+        constexpr bool kStage = kCols || kI8;
+        const uint32_t stg = sbase + L.stage + static_cast<uint32_t>(warp) * kStageBytes;
+        const float* stg_f = reinterpret_cast<const float*>(smem + L.stage + warp * kStageBytes);
+        auto stage_tile = [&](int t, int buf) {
+            const uint32_t d = stg + static_cast<uint32_t>(buf) * (2 * kHalfCols * 4);
+            const size_t col = static_cast<size_t>(t) * kRows + hc * kHalfCols;
+            if (kCols && lane < 16) cp_async16(d + lane * 16, lse_row + col + lane * 4);
+            if (kI8 && lane >= 16) cp_async16(d + kHalfCols * 4 + (lane - 16) * 16, str_scale + col + (lane - 16) * 4);
+            cp_async_commit();
+        };
+        if constexpr (kStage) stage_tile(t_lo, 0);
         for (int j = 0; j < nt; ++j) {
             const int s = j & 1;
             const uint32_t use = static_cast<uint32_t>(j >> 1);
+            if constexpr (kStage) {
+                if (j + 1 < nt) stage_tile(t_lo + j + 1, (j + 1) & 1);
+                else cp_async_commit();
+            }
             if (!mbar_wait(bar_mma(s), use & 1u)) {
                 if (lane == 0) {
                     set_status(a.status, QS_DEV_ETIMEOUT);
@@ -454,16 +488,21 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
                 break;
             }
             tc_fence_after();
+            if constexpr (kStage) {
+                cp_async_wait1();   // this tile's group (the next tile's may still fly)
+                __syncwarp();
+            }
+            const float* cur = stg_f + (j & 1) * (2 * kHalfCols);
             const int t = t_lo + j;
 #pragma unroll 1
             for (int c0 = hc * 64; c0 < hc * 64 + 64; c0 += 32) {
                 float v[32];
                 float sc[32];   // int8: the streamed rows' scales of these columns
                 if constexpr (kI8) {
-                    const float4* s4 = reinterpret_cast<const float4*>(str_scale + static_cast<size_t>(t) * kRows + c0);
+                    const float4* s4 = reinterpret_cast<const float4*>(cur + kHalfCols + (c0 - hc * 64));
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4) {
-                        const float4 w4 = __ldg(s4 + q4);
+                        const float4 w4 = s4[q4];
                         sc[4 * q4] = w4.x; sc[4 * q4 + 1] = w4.y; sc[4 * q4 + 2] = w4.z; sc[4 * q4 + 3] = w4.w;
                     }
                 }
@@ -497,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
                     }
                 } else {
                     // query rows pr = t*128 + c0 + jj with position >= key s, < S
-                    const float4* lse_s = reinterpret_cast<const float4*>(lse_row + static_cast<size_t>(t) * kRows + c0);
+                    const float4* lse_s = reinterpret_cast<const float4*>(cur + (c0 - hc * 64));
                     const int pr0 = t * kRows + c0;
                     const int pr_min = pr_res * G;     // first row of a position >= the key
                     const int pr_end = S * G;
@@ -505,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
                         float lse[32];
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4) {
-                            const float4 l4 = __ldg(lse_s + q4);
+                            const float4 l4 = lse_s[q4];
                             lse[4 * q4] = l4.x; lse[4 * q4 + 1] = l4.y;
                             lse[4 * q4 + 2] = l4.z; lse[4 * q4 + 3] = l4.w;
                         }
@@ -523,9 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1) importance_tc_kernel(const TcArgs
                 }
             }
             tc_fence_before();
-            __syncwarp();
+            __syncwarp();   // also: every lane has read this tile's staged values
             if (lane == 0) mbar_arrive(bar_empty(s));
         }
+        if constexpr (kStage) cp_async_wait0();
         // combine the two column halves of every row (the second half's
         // state goes through shared memory)
         float* half_m = reinterpret_cast<float*>(smem + L.half);
