@@ -105,9 +105,9 @@ def test_importance_matches_oracle(name):
         assert np.isclose(got[b].sum(), w.H * S, rtol=1e-5)
 
 
-def test_importance_table_beyond_staging_limit():
-    """BLOCK_SIZE 1 and 2100 tokens: more table entries than a CTA stages
-    (the keys' entries are then read from the table in global memory)."""
+def test_importance_block_size_one_long_table():
+    """BLOCK_SIZE 1 and 2100 tokens: the key packing follows one table entry
+    per key, 2100 entries, and the last key tile is partial."""
     w = PI.replace(B=1, H=2, N=1, D=64, BS=1, seq_len=None, ragged=(1, 2, 1), needle=False)
     lens = [2100]
     x, g, q, _ = inputs(w, lens, 3, DEV)
