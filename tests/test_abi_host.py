@@ -136,3 +136,36 @@ def test_step_kernels_query_without_gpu(built_lib):
     assert qs.step_kernels(p) == 2
     n = ctypes.c_int32(0)
     assert built_lib.qs_step_kernels(None, ctypes.byref(n)) == 1       # QS_EINVAL
+
+
+def header_enum_values():
+    """name -> value of every enumerator the header declares."""
+    txt = open(os.path.join(ROOT, "include", "questsparse.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    vals = {}
+    for body in re.findall(r"enum\s*\w*\s*\{(.*?)\}", txt, flags=re.S):
+        for name, v in re.findall(r"\b(QS_[A-Z0-9_]+)\s*=\s*(-?\d+)", body):
+            vals[name] = int(v)
+    return vals
+
+
+def test_binding_constants_match_the_header():
+    from decode_sparse_attention_gb300 import questsparse as qs
+    v = header_enum_values()
+    assert (qs.F32, qs.BF16, qs.F16, qs.I8) == (v["QS_F32"], v["QS_BF16"], v["QS_F16"], v["QS_I8"])
+    assert (qs.OP_BLOCK_SELECT, qs.OP_PROBE_SELECT, qs.OP_SPARSE_ATTN, qs.OP_STEP_QUEST,
+            qs.OP_STEP_PROBE) == (v["QS_OP_BLOCK_SELECT"], v["QS_OP_PROBE_SELECT"],
+                                  v["QS_OP_SPARSE_ATTN"], v["QS_OP_DECODE_STEP_QUEST"],
+                                  v["QS_OP_DECODE_STEP_PROBE"])
+    assert v["QS_OK"] == 0 and v["QS_DEV_OK"] == 0 and v["QS_DEV_ETIMEOUT"] == 6
+
+
+def test_device_status_strings_cover_every_code(built_lib):
+    """Every device-side code the header declares has its own message."""
+    built_lib.qs_status_string.restype = ctypes.c_char_p
+    built_lib.qs_status_string.argtypes = [ctypes.c_int32]
+    v = header_enum_values()
+    dev = sorted(val for name, val in v.items() if name.startswith("QS_DEV_E"))
+    msgs = [built_lib.qs_status_string(100 + c) for c in dev]
+    assert all(m and m != built_lib.qs_status_string(999) for m in msgs)
+    assert len(set(msgs)) == len(msgs)
