@@ -149,6 +149,21 @@ extern "C" qs_status qs_sparse_decode_step(const qs_step_params* p, qs_stream_t 
                             p->dev_status, s, /*pdl=*/true);
 }
 
+namespace {
+
+// Metadata rows of one unit that the one-CTA-per-unit Quest selector scores
+// in a single load step: 8 warps, a row per lane group of D*e/16 lanes, 8
+// rows in flight per group.  Units with more rows take the scan and then a
+// per-unit top-k kernel (the selector's launch rule).  0: no such kernel.
+int quest_unit_rows(qs_dtype meta_dtype, int32_t D) {
+    const int e = meta_dtype == QS_F32 ? 4 : 2;
+    const int lanes_per_row = D * e / 16;
+    if (D <= 0 || lanes_per_row <= 0 || lanes_per_row > 32 || 32 % lanes_per_row != 0) return 0;
+    return 8 * (32 / lanes_per_row) * 8;
+}
+
+}  // namespace
+
 extern "C" qs_status qs_step_kernels(const qs_step_params* p, int32_t* kernels) {
     using namespace qs;
     if (!p || !kernels) return QS_EINVAL;
@@ -160,6 +175,10 @@ extern "C" qs_status qs_step_kernels(const qs_step_params* p, int32_t* kernels) 
     bool fused = false;
     quest_step_fused(p, static_cast<uint8_t*>(p->workspace) + sel_ws, p->workspace_bytes - sel_ws,
                      nullptr, &fused, false);
-    if (fused) *kernels = 1;
+    if (fused) {
+        *kernels = 1;
+    } else if (static_cast<long long>(p->MMBPR) * p->BS > quest_unit_rows(p->kv_dtype, p->D)) {
+        *kernels = 3;   // scan + per-unit top-k + attention
+    }
     return QS_OK;
 }

@@ -321,9 +321,13 @@ typedef struct {
 qs_status qs_sparse_decode_step(const qs_step_params* params, qs_stream_t stream);
 
 /* How many kernels qs_sparse_decode_step(params) launches: 1 when it takes the
- * fused Quest kernel, else 2 (selector + attention).  Enqueues nothing and
- * reads no device memory.  Returns QS_EINVAL for a NULL argument,
- * QS_EWORKSPACE when the workspace is too small to hold the selector part. */
+ * fused Quest kernel; 3 when the Quest selector scans (a unit of more metadata
+ * rows, MMBPR*BS, than its one-CTA form scores in one load step: 128 rows at
+ * D = 128 with bf16/fp16 metadata, 64 with fp32; 256 and 128 at D = 64) and
+ * then ranks each unit in a second kernel, before the attention; else 2
+ * (selector + attention).  Enqueues nothing and reads no device memory.
+ * Returns QS_EINVAL for a NULL argument, QS_EWORKSPACE when the workspace is
+ * too small to hold the selector part. */
 qs_status qs_step_kernels(const qs_step_params* params, int32_t* kernels);
 
 /*

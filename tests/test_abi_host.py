@@ -138,6 +138,32 @@ def test_step_kernels_query_without_gpu(built_lib):
     assert built_lib.qs_step_kernels(None, ctypes.byref(n)) == 1       # QS_EINVAL
 
 
+def test_step_kernels_counts_the_scan_path(built_lib):
+    """A Quest step whose units have more metadata rows than the one-CTA
+    selector scores in one load step runs scan + per-unit top-k + attention:
+    three kernels (the ragged and long-context workloads), else two."""
+    from decode_sparse_attention_gb300 import questsparse as qs
+    ws = (ctypes.c_uint8 * 1024)()
+    cases = [
+        # kv dtype, D, MMBPR, BS -> kernels
+        (qs.BF16, 128, 1, 128, 2),     # bf16_paged: 128 rows, one chunk
+        (qs.F16, 128, 1, 128, 2),
+        (qs.BF16, 128, 4, 128, 3),     # long_context: 512 rows
+        (qs.BF16, 128, 8, 128, 3),     # ragged: up to 1024 rows
+        (qs.F32, 128, 1, 64, 2),       # fp32 rows are twice as wide: 64 rows per step
+        (qs.F32, 128, 1, 128, 3),
+        (qs.BF16, 64, 2, 128, 2),      # D = 64: 256 rows
+        (qs.BF16, 64, 3, 128, 3),
+        (qs.F32, 64, 1, 128, 2),
+    ]
+    for dt, D, MMBPR, BS, want in cases:
+        p = qs.StepParams()
+        p.mode, p.kv_dtype, p.q_dtype = 0, dt, dt
+        p.B, p.H, p.N, p.D, p.BS, p.k, p.MMBPR, p.fused_select = 4, 32, 8, D, BS, 8, MMBPR, 0
+        p.workspace, p.workspace_bytes = ctypes.addressof(ws), 1 << 40
+        assert qs.step_kernels(p) == want, (dt, D, MMBPR, BS)
+
+
 def header_enum_values():
     """name -> value of every enumerator the header declares."""
     txt = open(os.path.join(ROOT, "include", "questsparse.h")).read()
