@@ -127,6 +127,17 @@ def _req(t, name, dtype=None, dim=None):
     return t
 
 
+def _rows(t, name, B):
+    """t holds one row (or entry) per request: at least B of them."""
+    if t.shape[0] < B:
+        raise QuestSparseError("%s must have a row per request (%d < %d)" % (name, t.shape[0], B))
+
+
+def _shape(t, name, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise QuestSparseError("%s must be %s, got %s" % (name, list(shape), list(t.shape)))
+
+
 # ---------------------------------------------------------------------------
 # per-device scratch: the device status word and zero-initialised workspaces
 # ---------------------------------------------------------------------------
@@ -214,6 +225,8 @@ def quest_prefill_metadata(k_cache, seq_lens, block_tables, metadata_block_table
         if tuple(t.shape[1:]) != (BS, N, D):
             raise QuestSparseError("%s must be [num_meta, BS, N, D]" % nm)
     B = seq_lens.shape[0]
+    _rows(block_tables, "block_tables", B)
+    _rows(metadata_block_tables, "metadata_block_tables", B)
     rc = lib().qs_prefill_metadata(_ptr(k_cache), _dt(k_cache), P_, BS, N, D, _ptr(seq_lens), B,
                                    _ptr(block_tables), block_tables.shape[1],
                                    _ptr(metadata_block_tables), metadata_block_tables.shape[1],
@@ -241,6 +254,8 @@ def quest_update_metadata(k_cache, prev_lens, seq_lens, block_tables, metadata_b
     B = seq_lens.shape[0]
     if prev_lens.shape[0] != B:
         raise QuestSparseError("prev_lens and seq_lens must have one entry per request")
+    _rows(block_tables, "block_tables", B)
+    _rows(metadata_block_tables, "metadata_block_tables", B)
     rc = lib().qs_update_metadata(_ptr(k_cache), _dt(k_cache), P_, BS, N, D, _ptr(prev_lens),
                                   _ptr(seq_lens), B, _ptr(block_tables), block_tables.shape[1],
                                   _ptr(metadata_block_tables), metadata_block_tables.shape[1],
@@ -263,6 +278,8 @@ def quest_block_select_paged_in_out_w(query, maxblocks, minblocks, metadata_bloc
         raise QuestSparseError("head dim mismatch")
     _req(metadata_block_tables, "metadata_block_tables", torch.int32, 2)
     _req(seq_lens, "seq_lens", torch.int32, 1)
+    _rows(metadata_block_tables, "metadata_block_tables", B)
+    _rows(seq_lens, "seq_lens", B)
     _req(selected_indices, "selected_indices", torch.int32, 3)
     k = selected_indices.shape[2]
     if tuple(selected_indices.shape) != (B, N, k):
@@ -311,13 +328,18 @@ def probe_select(q, k_cache, block_tables, seq_lens, k, n_probe=8, importance=No
         raise QuestSparseError("head dim mismatch")
     _req(block_tables, "block_tables", torch.int32, 2)
     _req(seq_lens, "seq_lens", torch.int32, 1)
+    _rows(block_tables, "block_tables", B)
+    _rows(seq_lens, "seq_lens", B)
     if importance is not None:
         _req(importance, "importance", torch.float32, 2)
+        _rows(importance, "importance", B)
     if k_scale is not None:
         _req(k_scale, "k_scale", torch.float32, 3)
+        _shape(k_scale, "k_scale", (P_, BS, N))
     if selected is None:
         selected = torch.empty((B, H, k), dtype=torch.int32, device=q.device)
     _req(selected, "selected", torch.int32, 3)
+    _shape(selected, "selected", (B, H, k))
     MKBPR = block_tables.shape[1]
     nbytes = workspace_size(OP_PROBE_SELECT, B, H, N, D, BS, k, MKBPR, H)
     ws = workspace(nbytes, q.device, ("probe", B, H, N, D, BS, k, MKBPR))
@@ -354,13 +376,18 @@ def prefill_importance(q, k_cache, block_tables, prefill_lens, softmax_scale=Non
         raise QuestSparseError("head dim mismatch")
     _req(block_tables, "block_tables", torch.int32, 2)
     _req(prefill_lens, "prefill_lens", torch.int32, 1)
+    _rows(block_tables, "block_tables", B)
+    _rows(prefill_lens, "prefill_lens", B)
     if k_scale is not None:
         _req(k_scale, "k_scale", torch.float32, 3)
+        _shape(k_scale, "k_scale", (P_, BS, N))
     if importance is None:
         importance = torch.empty((B, S_max), dtype=torch.float32, device=q.device)
     _req(importance, "importance", torch.float32, 2)
+    _shape(importance, "importance", (B, S_max))
     if lse is not None:
         _req(lse, "lse", torch.float32, 3)
+        _shape(lse, "lse", (B, H, S_max))
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     nbytes = prefill_importance_workspace_size(B, H, N, D, S_max, _dt(k_cache))
@@ -387,13 +414,24 @@ def sparse_decode_attn(q, k_cache, v_cache, block_tables, seq_lens, selected, so
         raise QuestSparseError("cache shape mismatch")
     _req(block_tables, "block_tables", torch.int32, 2)
     _req(seq_lens, "seq_lens", torch.int32, 1)
+    _rows(block_tables, "block_tables", B)
+    _rows(seq_lens, "seq_lens", B)
     _req(selected, "selected", torch.int32, 3)
     sel_heads, k = selected.shape[1], selected.shape[2]
+    if selected.shape[0] != B or sel_heads not in (N, H):
+        raise QuestSparseError("selected must be [B, N, k] or [B, H, k]")
+    for t, nm in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t is not None:
+            _req(t, nm, torch.float32, 3)
+            _shape(t, nm, (P_, BS, N))
     if out is None:
         out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
     _req(out, "out", torch.float32, 3)
+    _shape(out, "out", (B, H, D))
     if lse is not None:
         _req(lse, "lse", torch.float32)
+        if lse.numel() != B * H:
+            raise QuestSparseError("lse must hold [B, H] floats")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     nbytes = workspace_size(OP_SPARSE_ATTN, B, H, N, D, BS, k, block_tables.shape[1], sel_heads)

@@ -195,3 +195,66 @@ def test_device_status_strings_cover_every_code(built_lib):
     msgs = [built_lib.qs_status_string(100 + c) for c in dev]
     assert all(m and m != built_lib.qs_status_string(999) for m in msgs)
     assert len(set(msgs)) == len(msgs)
+
+
+def test_binding_checks_sizes_before_any_call(built_lib, monkeypatch):
+    """Outputs and per-request inputs of the wrong size are refused by the
+    binding before the library is called (the C ABI trusts its sizes).  The
+    device placement check is switched off so host tensors reach them."""
+    from decode_sparse_attention_gb300 import questsparse as qs
+
+    def req_no_device(t, name, dtype=None, dim=None):
+        if dtype is not None and t.dtype != dtype:
+            raise qs.QuestSparseError("%s must be %s" % (name, dtype))
+        if dim is not None and t.dim() != dim:
+            raise qs.QuestSparseError("%s must have %d dims" % (name, dim))
+        return t
+
+    def no_call(*a, **k):
+        raise AssertionError("the library was called")
+
+    monkeypatch.setattr(qs, "_req", req_no_device)
+    monkeypatch.setattr(qs, "lib", no_call)
+    monkeypatch.setattr(qs, "workspace_size", no_call)
+    monkeypatch.setattr(qs, "prefill_importance_workspace_size", no_call)
+    i32 = torch.int32
+    B, H, N, D, BS, k = 3, 8, 2, 64, 16, 4
+    q = torch.zeros(B, H, D, dtype=torch.bfloat16)
+    kc = torch.zeros(10, BS, N, D, dtype=torch.bfloat16)
+    bt = torch.zeros(B, 5, dtype=i32)
+    sl = torch.zeros(B, dtype=i32)
+    sel = torch.zeros(B, N, k, dtype=i32)
+    E = qs.QuestSparseError
+    with pytest.raises(E, match="row per request"):
+        qs.sparse_decode_attn(q, kc, kc, bt[:2], sl, sel)
+    with pytest.raises(E, match="row per request"):
+        qs.sparse_decode_attn(q, kc, kc, bt, sl[:2], sel)
+    with pytest.raises(E, match="selected"):
+        qs.sparse_decode_attn(q, kc, kc, bt, sl, torch.zeros(B, 3, k, dtype=i32))
+    with pytest.raises(E, match="out must be"):
+        qs.sparse_decode_attn(q, kc, kc, bt, sl, sel, out=torch.zeros(B, H, D // 2))
+    with pytest.raises(E, match="lse"):
+        qs.sparse_decode_attn(q, kc, kc, bt, sl, sel, lse=torch.zeros(B, H - 1))
+    with pytest.raises(E, match="v_scale must be"):
+        qs.sparse_decode_attn(q, kc, kc, bt, sl, sel, v_scale=torch.zeros(10, BS, N + 1))
+    with pytest.raises(E, match="selected must be"):
+        qs.probe_select(q, kc, bt, sl, k, selected=torch.zeros(B, N, k, dtype=i32))
+    with pytest.raises(E, match="row per request"):
+        qs.probe_select(q, kc, bt, sl, k, importance=torch.zeros(B - 1, 80))
+    with pytest.raises(E, match="k_scale must be"):
+        qs.probe_select(q, kc, bt, sl, k, k_scale=torch.zeros(10, BS, 1))
+    qp = torch.zeros(B, 80, H, D, dtype=torch.bfloat16)
+    with pytest.raises(E, match="lse must be"):
+        qs.prefill_importance(qp, kc, bt, sl, lse=torch.zeros(B, H, 79))
+    with pytest.raises(E, match="importance must be"):
+        qs.prefill_importance(qp, kc, bt, sl, importance=torch.zeros(B, 81))
+    with pytest.raises(E, match="row per request"):
+        qs.prefill_importance(qp, kc, bt, sl[:1])
+    mx = torch.zeros(6, BS, N, D, dtype=torch.bfloat16)
+    with pytest.raises(E, match="row per request"):
+        qs.quest_prefill_metadata(kc, sl, bt, torch.zeros(B - 1, 2, dtype=i32), mx, mx)
+    with pytest.raises(E, match="row per request"):
+        qs.quest_update_metadata(kc, sl, sl, bt[:1], torch.zeros(B, 2, dtype=i32), mx, mx)
+    with pytest.raises(E, match="row per request"):
+        qs.quest_block_select_paged_in_out_w(q, mx, mx, torch.zeros(B, 2, dtype=i32), sl[:2], 0,
+                                             sel)
