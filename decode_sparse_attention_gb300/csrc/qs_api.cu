@@ -155,11 +155,14 @@ namespace {
 // in a single load step: 8 warps, a row per lane group of D*e/16 lanes, 8
 // rows in flight per group.  Units with more rows take the scan and then a
 // per-unit top-k kernel (the selector's launch rule).  0: no such kernel.
+constexpr int kUnitSelectWarps = 8;        // 256 threads per unit CTA
+constexpr int kUnitSelectRowsInFlight = 8;  // rows in flight per lane group
+
 int quest_unit_rows(qs_dtype meta_dtype, int32_t D) {
     const int e = meta_dtype == QS_F32 ? 4 : 2;
     const int lanes_per_row = D * e / 16;
     if (D <= 0 || lanes_per_row <= 0 || lanes_per_row > 32 || 32 % lanes_per_row != 0) return 0;
-    return 8 * (32 / lanes_per_row) * 8;
+    return kUnitSelectWarps * (32 / lanes_per_row) * kUnitSelectRowsInFlight;
 }
 
 }  // namespace

@@ -258,3 +258,18 @@ def test_binding_checks_sizes_before_any_call(built_lib, monkeypatch):
     with pytest.raises(E, match="row per request"):
         qs.quest_block_select_paged_in_out_w(q, mx, mx, torch.zeros(B, 2, dtype=i32), sl[:2], 0,
                                              sel)
+
+
+def test_step_kernel_rule_follows_the_selector_constants():
+    """qs_step_kernels restates the unit selector's one-step row count; its
+    constants must stay those of the selector's launch rule."""
+    csrc = os.path.join(ROOT, "decode_sparse_attention_gb300", "csrc")
+    sel = open(os.path.join(csrc, "qs_select.cu")).read()
+    api = open(os.path.join(csrc, "qs_api.cu")).read()
+    threads = int(re.search(r"constexpr int kThreads = (\d+);", sel).group(1))
+    unroll = int(re.search(r"constexpr int kUnroll = (\d+);", sel).group(1))
+    assert "(kThreads / 32) * (32 / (D * DtInfo<MT>::bytes / 16)) * kUnroll" in sel
+    assert "if (maxnb <= kRows)" in sel
+    warps = int(re.search(r"constexpr int kUnitSelectWarps = (\d+);", api).group(1))
+    in_flight = int(re.search(r"constexpr int kUnitSelectRowsInFlight = (\d+);", api).group(1))
+    assert (warps, in_flight) == (threads // 32, unroll)
